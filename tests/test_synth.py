@@ -1,0 +1,55 @@
+"""The shared input generator: determinism, ranges and dtype rounding."""
+import numpy as np
+import torch
+
+import synth
+
+
+def test_draws_are_counter_based_and_deterministic():
+    a = synth.draws_u64(3, 11, 100)
+    b = synth.draws_u64(3, 11, 40, start=60)
+    np.testing.assert_array_equal(a[60:], b)
+    assert not np.array_equal(a, synth.draws_u64(4, 11, 100))
+    assert not np.array_equal(a, synth.draws_u64(3, 12, 100))
+
+
+def test_splitmix64_reference_values():
+    # splitmix64 seeded with 0: first outputs of the published generator
+    # (state += 0x9E3779B97F4A7C15; z = mix(state)).
+    with np.errstate(over="ignore"):
+        got = [int(synth.mix64(np.uint64(k) * synth.GOLDEN)) for k in (1, 2, 3)]
+    assert got[0] == 0xE220A8397B1DCDAF
+    assert got[1] == 0x6E789E6AA1B965F4
+    assert got[2] == 0x06C45D188009454F
+
+
+def test_uniform_bytes_cover_range():
+    u = synth.uniform_u8(0, 1, 200000)
+    assert u.min() == 0 and u.max() == 255
+    assert abs(u.mean() - 127.5) < 1.0
+
+
+def test_normal_moments():
+    z = synth.normal(0, 2, 400000, 0.02)
+    assert abs(z.mean()) < 2e-4
+    assert abs(z.std() - 0.02) < 2e-4
+
+
+def test_bf16_and_f16_rounding_match_torch():
+    x = synth.normal(1, 3, 10000, 1.0).astype(np.float32) * 37.0
+    b = synth.round_to_dtype(x, "bf16")
+    np.testing.assert_array_equal(b, torch.from_numpy(x).bfloat16().float().numpy())
+    h = synth.round_to_dtype(x, "f16")
+    np.testing.assert_array_equal(h, torch.from_numpy(x).half().float().numpy())
+
+
+def test_workload_shapes():
+    c = synth.CONFIGS
+    assert synth.tokens_per_clip(c["c1"]) == 128
+    assert synth.tokens_per_clip(c["c3"]) == 2048
+    assert synth.tokens_per_clip(c["c4"]) == 8192
+    assert synth.tokens_per_clip(c["c5"]) == 18432
+    w = synth.encoder_weights(c["c1"])
+    assert w["patch_embed.weight"].shape == (768, 1536)
+    assert w["blk.0.attn_qkv.weight"].shape == (2304, 768)
+    assert np.all(w["blk.0.ln1.weight"] == 1) and np.all(w["blk.0.attn_qkv.bias"] == 0)
