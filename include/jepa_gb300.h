@@ -1,0 +1,247 @@
+/*
+ * jepa_gb300.h - C ABI of the GB300 (sm_103a) V-JEPA 2 / 2.1 video ViT encoder.
+ *
+ * The library computes the forward pass of the V-JEPA 2 / 2.1 video ViT
+ * encoder ("V-JEPA 2 / 2.1 tensor maps and RoPE derivation", §2 block form,
+ * §3 2.1 encoder forward, §4 3-D RoPE) and of the V-JEPA 2 masked predictor
+ * (same page, §2 key map, §3 predictor forward, §4.4 predictor ids), on one
+ * GPU, in hand-written CUDA kernels.
+ *
+ * Conventions for every entry point:
+ *   - Buffers documented as device buffers are CUDA device pointers owned by
+ *     the caller.  Pointers documented as host pointers are host memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device work is enqueued asynchronously on it; the call returns
+ *     once the work is enqueued unless the entry point says otherwise.
+ *   - Every function returns a jepa_status.  Argument errors are found on the
+ *     host before anything is launched; nothing is enqueued then.  The
+ *     message of the calling thread's last non-OK status is returned by
+ *     jepa_last_error().  No C++ exception crosses this boundary.
+ *   - Bounded device waits: kernels that wait on an mbarrier give up after a
+ *     time limit and set a device status word instead of hanging; the next
+ *     jepa_encoder_sync / jepa_predictor_sync reports it as
+ *     JEPA_ERR_DEVICE_TIMEOUT.
+ *   - Layouts are row-major, innermost dimension last.
+ *   - Calls on one handle must not overlap in time (a handle owns one
+ *     workspace).
+ */
+#ifndef JEPA_GB300_H
+#define JEPA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define JEPA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define JEPA_API __attribute__((visibility("default")))
+#else
+#define JEPA_API
+#endif
+
+typedef enum {
+  JEPA_OK = 0,
+  JEPA_ERR_ARG = 1,            /* bad argument (null pointer, size, unsupported shape)      */
+  JEPA_ERR_BLOB = 2,           /* weight blob truncated, wrong magic, or tensor mismatch    */
+  JEPA_ERR_UNSUPPORTED = 3,    /* valid but not implemented (e.g. head_dim not 32 or 64)    */
+  JEPA_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed                         */
+  JEPA_ERR_OOM = 5,            /* device allocation failed                                  */
+  JEPA_ERR_DEVICE_TIMEOUT = 6  /* a kernel gave up waiting on a barrier (reported at sync)  */
+} jepa_status;
+
+typedef enum { JEPA_DT_F32 = 0, JEPA_DT_F16 = 1, JEPA_DT_BF16 = 2 } jepa_dtype;
+typedef enum { JEPA_ROPE_TILED = 0, JEPA_ROPE_INTERLEAVED = 1 } jepa_rope_layout;
+typedef enum { JEPA_CLIP_U8_THWC = 0, JEPA_CLIP_F32_CTHW = 1 } jepa_clip_format;
+
+/* Encoder hyper-parameters ("V-JEPA 2 / 2.1 tensor maps and RoPE derivation",
+ * §1).  head_dim = embed_dim / n_head must be 32 or 64.  patch must be 16 and
+ * tubelet 2 (the Conv3d [D,3,2,16,16] of §2).  rope_layout: tiled (V-JEPA 2,
+ * §4.1) or interleaved (V-JEPA 2.1, §4.2).  rope_interpolate rescales spatial
+ * positions by (rope_ref_grid-1)/(n-1) (§4.3).  hier_layers (0-based block
+ * indices, increasing) select the hierarchical LayerNorm taps (§3).
+ * has_mod_embed adds the 2.1 video modality vector after the patch embed (§3).
+ * dtype: storage type of the 2-D matrices and of the activations fed to the
+ * matrix multiplies (F32 = fp32 CUDA-core path; F16/BF16 = tensor-core path
+ * with fp32 accumulation).  The residual stream, LayerNorm statistics,
+ * softmax and all outputs are fp32 in every mode. */
+typedef struct jepa_encoder_params {
+  int embed_dim, n_layer, n_head, ffn_dim;
+  int patch, tubelet;
+  float ln_eps, rope_theta;
+  int rope_layout, rope_interpolate, rope_ref_grid;
+  int n_hier;
+  int hier_layers[4];
+  int has_mod_embed;
+  int dtype;
+} jepa_encoder_params;
+
+/* Masked predictor hyper-parameters (same page, §1 "pred.*" rows).
+ * in_dim = encoder width; out_dim = projection width; the mask token used for
+ * every target row is mask_tokens[mask_index % n_mask_tokens]. */
+typedef struct jepa_predictor_params {
+  int embed_dim, n_layer, n_head, ffn_dim;
+  int in_dim, out_dim, n_mask_tokens, mask_index;
+  float ln_eps, rope_theta;
+  int rope_layout;
+  int dtype;
+} jepa_predictor_params;
+
+/* ---------------------------------------------------------------- weight blob
+ * Little-endian.  Header: char magic[8] = "JEPAGB3\0", uint32 version (1),
+ * uint32 n_tensors, uint64 reserved, then n_tensors entries of
+ * {uint64 offset, uint64 nbytes, uint32 dtype, uint32 ndim, uint32 dim0,
+ *  uint32 dim1} (offset from the blob start, 256-byte aligned).
+ * Encoder tensor order (names of §2 of the conversion notes):
+ *   patch_embed.weight [D,1536] (feature order C,T,H,W), patch_embed.bias [D],
+ *   [mod_embed_video [D] if has_mod_embed],
+ *   per block i: ln1.weight, ln1.bias [D], attn_qkv.weight [3D,D] (rows q;k;v),
+ *   attn_qkv.bias [3D], attn_out.weight [D,D], attn_out.bias [D],
+ *   ln2.weight, ln2.bias [D], ffn_up.weight [F,D], ffn_up.bias [F],
+ *   ffn_down.weight [D,F], ffn_down.bias [D];
+ *   norm.weight, norm.bias [D]; then hier_norm.k.weight/bias [D] per tap.
+ * Predictor order: embed.weight [D,in_dim], embed.bias [D], mask_tokens
+ *   [n_mask,D] (fp32), the blocks as above, norm.weight/bias, proj.weight
+ *   [out_dim,D], proj.bias [out_dim].
+ * 2-D matrices are stored in params.dtype, everything else in F32. */
+
+/* Host-only validation of a blob against params (no GPU needed). */
+JEPA_API jepa_status jepa_blob_check(const void* blob, size_t blob_bytes, const jepa_encoder_params* params);
+JEPA_API jepa_status jepa_predictor_blob_check(const void* blob, size_t blob_bytes, const jepa_predictor_params* params);
+
+/* ---------------------------------------------------------------- encoder
+ * jepa_encoder_create: validates params and the host blob, makes `device`
+ * current, copies the weights to device memory (owned by the handle until
+ * jepa_encoder_destroy).  The blob may be freed after the call. */
+typedef struct jepa_encoder jepa_encoder;
+JEPA_API jepa_status jepa_encoder_create(const void* blob, size_t blob_bytes, const jepa_encoder_params* params,
+                                int device, jepa_encoder** out);
+JEPA_API void jepa_encoder_destroy(jepa_encoder* enc);
+
+/* Bytes of device workspace jepa_encode allocates (once, grown on demand)
+ * for this clip shape; 0 on invalid arguments. */
+JEPA_API size_t jepa_encode_workspace_bytes(const jepa_encoder* enc, int batch, int n_frames, int height, int width);
+
+/* jepa_encode: last_hidden_state of `batch` independent clips.
+ *   clip: device buffer, JEPA_CLIP_U8_THWC: uint8 [batch, n_frames, H, W, 3]
+ *         raw pixels, normalised inside with the ImageNet mean/std in the
+ *         fused form (px - 255*mean)/(255*std) ("Parity ...", Preprocessing
+ *         parity); JEPA_CLIP_F32_CTHW: float [batch, 3, n_frames, H, W]
+ *         already normalised.
+ *   n_frames even, H and W multiples of 16 (non-square allowed), H/16 > 1 and
+ *   W/16 > 1 when interpolating RoPE.  N = (n_frames/2)*(H/16)*(W/16).
+ *   out_tokens: device float [batch, N, D] = enc.norm(x) (required).
+ *   out_pooled: device float [batch, D] token mean of out_tokens, or NULL.
+ *   out_hier:   device float [n_hier, batch, N, D] hierarchical taps, or NULL.
+ * The handle allocates its device workspace on the first call with a larger
+ * shape (JEPA_ERR_OOM if that fails). */
+JEPA_API jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_format, int batch, int n_frames,
+                        int height, int width, float* out_tokens, float* out_pooled, float* out_hier,
+                        void* stream);
+
+/* Same computation from and to HOST buffers (pinned memory is fastest): copies
+ * the clip to the device, encodes, copies out_tokens (and out_pooled if not
+ * NULL) back, and synchronises `stream` before returning. */
+JEPA_API jepa_status jepa_encode_host(jepa_encoder* enc, const void* host_clip, int clip_format, int batch,
+                             int n_frames, int height, int width, float* host_out_tokens,
+                             float* host_out_pooled, void* stream);
+
+/* The two halves of jepa_encode, for checking one stage at a time:
+ * jepa_encoder_embed writes the patch embedding (+ modality vector) of the
+ * clip into x_out, device float [batch*N, D]; jepa_encoder_blocks runs blocks
+ * [layer_begin, layer_end) in place on x (device float [batch*N, D]) for the
+ * given clip geometry. */
+JEPA_API jepa_status jepa_encoder_embed(jepa_encoder* enc, const void* clip, int clip_format, int batch, int n_frames,
+                               int height, int width, float* x_out, void* stream);
+JEPA_API jepa_status jepa_encoder_blocks(jepa_encoder* enc, float* x, int batch, int n_frames, int height, int width,
+                                int layer_begin, int layer_end, void* stream);
+
+/* Synchronises `stream` and reports a device-side timeout recorded by any
+ * earlier call on this handle (then clears it). */
+JEPA_API jepa_status jepa_encoder_sync(jepa_encoder* enc, void* stream);
+
+/* Per-kernel-class device time of the calls made while profiling is on,
+ * measured with CUDA events recorded on the call's stream around every
+ * launch.  Classes: 0 patch embed, 1 LayerNorm, 2 QKV GEMM, 3 attention,
+ * 4 out-proj GEMM, 5 FFN-up GEMM, 6 FFN-down GEMM, 7 other.  times_ms[8] and
+ * launches[8] are host arrays (either may be NULL); reading synchronises. */
+JEPA_API jepa_status jepa_encoder_set_profiling(jepa_encoder* enc, int on);
+JEPA_API jepa_status jepa_encoder_profile(jepa_encoder* enc, double* times_ms, long long* launches, int reset);
+
+/* ---------------------------------------------------------------- predictor
+ * jepa_predict: V-JEPA 2 masked predictor over one clip's encoder tokens.
+ *   enc_tokens: device float [n_tokens, in_dim] (the encoder's output);
+ *   ids_ctx [n_ctx], ids_tgt [n_tgt]: device int32 token ids in the encoder
+ *   grid grid_t x grid_h x grid_w (T-major), each < n_tokens;
+ *   out: device float [n_tgt, out_dim] = pred.proj(pred.norm(z))[n_ctx:]. */
+typedef struct jepa_predictor jepa_predictor;
+JEPA_API jepa_status jepa_predictor_create(const void* blob, size_t blob_bytes, const jepa_predictor_params* params,
+                                  int device, jepa_predictor** out);
+JEPA_API void jepa_predictor_destroy(jepa_predictor* pred);
+JEPA_API jepa_status jepa_predict(jepa_predictor* pred, const float* enc_tokens, int n_tokens, const int32_t* ids_ctx,
+                         int n_ctx, const int32_t* ids_tgt, int n_tgt, int grid_t, int grid_h, int grid_w,
+                         float* out, void* stream);
+JEPA_API jepa_status jepa_predictor_sync(jepa_predictor* pred, void* stream);
+
+/* ---------------------------------------------------------------- single operations
+ * The kernels of the encoder, callable one at a time (the same code runs
+ * inside jepa_encode).  All buffers are device buffers. */
+
+/* LayerNorm over the last dimension, biased centred variance, eps inside the
+ * square root ("V-JEPA 2 / 2.1 ...", §1 ln_eps; "Parity ...", Parity on a
+ * GPU: two-pass variance).  x, y: float [rows, dim]; w, b: float [dim].
+ * dim % 128 == 0 and dim <= 4096.  In place (y == x) is allowed. */
+JEPA_API jepa_status jepa_layernorm_f32(const float* x, const float* w, const float* b, float* y, int rows, int dim,
+                               float eps, void* stream);
+
+/* 3-D RoPE in place on x: float [batch, n_tokens, n_head*head_dim] (q or k,
+ * heads concatenated), positions of token i decoded T-major from the grid
+ * grid_t x grid_h x grid_w with n_tokens = grid_t*grid_h*grid_w ("V-JEPA 2 /
+ * 2.1 ...", §4: split d = 2*((head_dim//3)//2), §4.1 tiled, §4.2 interleaved,
+ * §4.3 interpolation).  head_dim 32 or 64. */
+JEPA_API jepa_status jepa_rope3d_f32(float* x, int batch, int n_tokens, int n_head, int head_dim, int grid_t, int grid_h,
+                            int grid_w, int layout, int interpolate, int ref_grid, float theta, void* stream);
+
+/* Unmasked softmax attention, softmax(scale * q k^T) v per (clip, head)
+ * ("V-JEPA 2 / 2.1 ...", §2 concat_heads, §4: scale 1/sqrt(head_dim)).
+ *   q, k: dtype [batch*n_head, n_tokens, head_dim];
+ *   vt:   dtype [batch*n_head, head_dim, ldv] (V transposed, ldv >= n_tokens,
+ *         ldv % 8 == 0, padding columns finite);
+ *   out:  dtype [batch, n_tokens, n_head*head_dim] (heads concatenated).
+ * head_dim 32 or 64; fp32 softmax statistics and accumulators. */
+JEPA_API jepa_status jepa_attention(const void* q, const void* k, const void* vt, void* out, int dtype, int batch,
+                           int n_head, int n_tokens, int head_dim, int ldv, float scale, void* stream);
+
+/* Linear layer out = A W^T + bias with a fused epilogue, fp32 accumulation.
+ *   A: dtype [M, K]; W: dtype [N, K]; bias: float [N] or NULL.
+ *   epilogue 0: out dtype [M, N] = acc + bias
+ *            1: out float [M, N] = acc + bias
+ *            2: out float [M, N] += acc + bias   (residual add in place)
+ *            3: out dtype [M, N] = gelu_erf(acc + bias)
+ * F16/BF16 (tensor cores): K % 64 == 0, N % 32 == 0.  F32: K % 16 == 0,
+ * N % 4 == 0. */
+JEPA_API jepa_status jepa_linear(const void* A, const void* W, const float* bias, void* out, int M, int N, int K, int dtype,
+                        int epilogue, void* stream);
+
+/* Synchronises `stream` and reports a device-side timeout recorded by any
+ * earlier single-operation call (jepa_attention, jepa_linear) of this process
+ * (then clears it). */
+JEPA_API jepa_status jepa_ops_sync(void* stream);
+
+/* Failure-detection self test: launches one kernel that waits on a barrier
+ * that nothing completes, with a limit of timeout_us microseconds, then
+ * synchronises.  Returns JEPA_ERR_DEVICE_TIMEOUT when the kernel reported
+ * the expired wait (the expected outcome); the context stays usable. */
+JEPA_API jepa_status jepa_selftest_wait_timeout(int timeout_us, void* stream);
+
+/* Message of the calling thread's last non-OK status ("" if none). */
+JEPA_API const char* jepa_last_error(void);
+JEPA_API int jepa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* JEPA_GB300_H */

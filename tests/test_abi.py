@@ -1,0 +1,100 @@
+"""The C ABI on the host: the library builds, loads and exports every entry
+point the header declares; blob and argument validation (no GPU needed)."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "jepa_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from video_vit_encoder_gb300 import build
+    build.build()
+    import video_vit_encoder_gb300 as jg
+    return jg.load()
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"^JEPA_API [^(]*?\b(jepa_\w+)\(", txt, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 20
+    from video_vit_encoder_gb300._lib import SIGNATURES
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in SIGNATURES, f"binding lacks {n}"
+    assert lib.jepa_abi_version() == 1
+
+
+def _blob(cfg):
+    import video_vit_encoder_gb300 as jg
+    w = synth.encoder_weights(cfg)
+    return jg.pack_blob(jg.encoder_tensor_order(cfg), w, cfg.dtype)
+
+
+def test_blob_roundtrip_and_faults(lib):
+    import video_vit_encoder_gb300 as jg
+    from video_vit_encoder_gb300._lib import JepaError, ERR_BLOB, ERR_ARG, ERR_UNSUPPORTED
+    cfg = synth.CONFIGS["c1"].with_(n_layer=2, dtype="bf16")
+    blob = _blob(cfg)
+    jg.blob_check(cfg, blob)                       # valid
+    with pytest.raises(JepaError) as e:            # truncated
+        jg.blob_check(cfg, blob[: len(blob) - 100])
+    assert e.value.status == ERR_BLOB
+    bad = bytearray(blob); bad[0] = ord("X")       # wrong magic
+    with pytest.raises(JepaError) as e:
+        jg.blob_check(cfg, bytes(bad))
+    assert e.value.status == ERR_BLOB
+    with pytest.raises(JepaError) as e:            # parameters that do not match the blob
+        jg.blob_check(cfg.with_(n_layer=3), blob)
+    assert e.value.status == ERR_BLOB
+    with pytest.raises(JepaError) as e:            # dtype mismatch
+        jg.blob_check(cfg.with_(dtype="f16"), blob)
+    assert e.value.status == ERR_BLOB
+    with pytest.raises(JepaError) as e:            # unsupported head dim
+        jg.blob_check(cfg.with_(n_head=6), blob)
+    assert e.value.status == ERR_UNSUPPORTED
+    with pytest.raises(JepaError) as e:            # bad hierarchical taps
+        jg.blob_check(cfg.with_(hier_layers=(1, 1)), blob)
+    assert e.value.status == ERR_ARG
+
+
+def test_blob_layout_is_aligned(lib):
+    import struct
+    cfg = synth.CONFIGS["c1"].with_(dtype="f16")
+    blob = _blob(cfg)
+    assert blob[:8] == b"JEPAGB3\0"
+    ver, n = struct.unpack_from("<II", blob, 8)
+    assert ver == 1 and n == 2 + 12 + 2
+    for i in range(n):
+        off, nb, dt, nd, d0, d1 = struct.unpack_from("<QQIIII", blob, 24 + 32 * i)
+        assert off % 256 == 0 and off + nb <= len(blob)
+    # first tensor is the patch embedding in fp16, matching the generator's values
+    off, nb, dt, nd, d0, d1 = struct.unpack_from("<QQIIII", blob, 24)
+    assert (dt, nd, d0, d1) == (1, 2, 768, 1536)
+    w = synth.encoder_weights(cfg)["patch_embed.weight"]
+    got = np.frombuffer(blob, np.float16, count=d0 * d1, offset=off).astype(np.float32).reshape(d0, d1)
+    np.testing.assert_array_equal(got, w)
+
+
+def test_argument_errors_without_gpu(lib):
+    # Host-side validation happens before any CUDA call.
+    from video_vit_encoder_gb300._lib import ERR_ARG, ERR_UNSUPPORTED
+    assert lib.jepa_layernorm_f32(None, None, None, None, 4, 128, 1e-6, None) == ERR_ARG
+    assert lib.jepa_rope3d_f32(C.c_void_p(16), 1, 10, 1, 48, 1, 2, 5, 0, 0, 16, 1e4, None) == ERR_UNSUPPORTED
+    assert lib.jepa_rope3d_f32(C.c_void_p(16), 1, 11, 1, 64, 1, 2, 5, 0, 0, 16, 1e4, None) == ERR_ARG
+    assert lib.jepa_linear(C.c_void_p(16), C.c_void_p(16), None, C.c_void_p(16), 8, 32, 40, 2, 0, None) == ERR_ARG
+    assert lib.jepa_attention(C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), 2, 1, 1, 100, 64,
+                              100, 0.125, None) == ERR_ARG          # ldv not a multiple of 8
+    assert lib.jepa_encoder_sync(None, None) == ERR_ARG
+    assert b"NULL" in lib.jepa_last_error()

@@ -1,0 +1,276 @@
+// Device-side helpers shared by the kernels: dtype traits, PTX wrappers for
+// mbarrier / TMA / tcgen05 (sm_103a), bounded barrier waits, RoPE tables.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+namespace jepa {
+
+// ----------------------------------------------------------------------------- status word
+// Bits set by a kernel in the handle's device status word.
+enum : int { DEV_TIMEOUT = 1 };
+// A wait on a barrier gives up after this many nanoseconds (a correct kernel
+// never waits more than microseconds).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// ----------------------------------------------------------------------------- dtypes
+template <typename T> struct DT;
+template <> struct DT<float> {
+  static __device__ __forceinline__ float to(float x) { return x; }
+  static __device__ __forceinline__ float from(float x) { return x; }
+};
+template <> struct DT<__nv_bfloat16> {
+  static __device__ __forceinline__ float to(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from(float x) { return __float2bfloat16_rn(x); }
+};
+template <> struct DT<__half> {
+  static __device__ __forceinline__ float to(__half x) { return __half2float(x); }
+  static __device__ __forceinline__ __half from(float x) { return __float2half_rn(x); }
+};
+
+// Packs two floats into one 32-bit word of two 16-bit values (low half = a).
+template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+  __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <typename T> __device__ __forceinline__ float2 unpack2(uint32_t u);
+template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
+}
+template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t u) {
+  return __half22float2(*reinterpret_cast<__half2*>(&u));
+}
+
+// Exact-erf GELU, 0.5 z (1 + erf(z / sqrt 2)).
+__device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+
+// ----------------------------------------------------------------------------- misc PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ----------------------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of parity `parity` to complete.  Returns false if it
+// did not within limit_ns (the caller then records a timeout and winds down
+// instead of spinning forever).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ----------------------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// ----------------------------------------------------------------------------- tcgen05
+// Tensor-memory allocation (the whole warp executes these).
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 or fp16 inputs, fp32 accumulator).
+__device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives once on `bar` when all tcgen05 operations issued so far by this thread complete.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane
+// (base lane + i), columns [col, col+32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile whose rows are
+// exactly one swizzle atom wide (128-byte rows with the 128B swizzle, or
+// 64-byte rows with the 64B swizzle), 8-row atoms stacked contiguously (the
+// layout a TMA tile load with that swizzle writes).  Fields: start address
+// >> 4 (bits 0-13), leading byte offset >> 4 (bits 16-29; not used by this
+// layout, set to 1), stride byte offset >> 4 (bits 32-45: distance between
+// 8-row groups), version 1 (bits 46-47), base offset 0 (bits 49-51), layout
+// type (bits 61-63: 2 = 128B swizzle, 4 = 64B swizzle).  Advancing along K
+// inside the atom is done by adding the byte offset to the start address.
+template <int kRowBytes>
+__device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr) {
+  static_assert(kRowBytes == 128 || kRowBytes == 64, "row width must be one swizzle atom");
+  constexpr uint64_t layout = kRowBytes == 128 ? 2ull : 4ull;
+  constexpr uint64_t sbo = (8ull * kRowBytes) >> 4;
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (sbo << 32) | (1ull << 46) | (layout << 61);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
+// 4-5 = 1), A and B type (bits 7-9 and 10-12: 0 fp16, 1 bf16), both operands
+// K-major (bits 15, 16 = 0), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+template <typename T, int M, int N>
+__host__ __device__ constexpr uint32_t idesc_f16() {
+  static_assert(M == 64 || M == 128, "M");
+  static_assert(N % 16 == 0 && N >= 16 && N <= 256, "N");
+  constexpr uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ----------------------------------------------------------------------------- RoPE
+// Per-axis angle tables built on the host in double and rounded to float:
+// cos_tab[(a * max_pos + p) * half + k] = cos(pos_a(p) * omega_k) for axis a
+// (0 = t, 1 = h, 2 = w), grid index p, k < half = d/2, where pos_a(p) is the
+// (possibly interpolated) position of grid index p.
+struct RopeParams {
+  const float* cos_tab;
+  const float* sin_tab;
+  int max_pos;      // stride of the position index
+  int d;            // rotated width per axis
+  int layout;       // 0 tiled, 1 interleaved
+  int gt, gh, gw;   // grid for decoding a token id
+};
+
+// Rotates the pairs (dim0 + j, dim0 + j + 1), j = 0, 2, .., n-2, of one head
+// row held in v (fp32) for the token at grid cell (t, h, w):
+// out[2k] = x[2k] c - x[2k+1] s, out[2k+1] = x[2k+1] c' + x[2k] s', where the
+// angle index of dim j in axis segment a is (j mod d/2) for the tiled layout
+// and (j div 2) for the interleaved one.  dim0 must be even.
+template <int n>
+__device__ __forceinline__ void rope_apply(float* v, int dim0, const RopeParams& rp, int t, int h, int w) {
+  const int d = rp.d, half = d >> 1;
+#pragma unroll
+  for (int j = 0; j < n; j += 2) {
+    const int dim = dim0 + j;
+    if (dim < 3 * d) {
+      const int a = dim / d;
+      const int jj = dim - a * d;
+      const int p = a == 0 ? t : (a == 1 ? h : w);
+      int f0, f1;
+      if (rp.layout == 0) {
+        f0 = jj % half;
+        f1 = (jj + 1) % half;
+      } else {
+        f0 = f1 = jj >> 1;
+      }
+      const float* ct = rp.cos_tab + (a * rp.max_pos + p) * half;
+      const float* st = rp.sin_tab + (a * rp.max_pos + p) * half;
+      const float c0 = __ldg(ct + f0), s0 = __ldg(st + f0), c1 = __ldg(ct + f1), s1 = __ldg(st + f1);
+      const float x0 = v[j], x1 = v[j + 1];
+      v[j] = x0 * c0 - x1 * s0;
+      v[j + 1] = x1 * c1 + x0 * s1;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------- GEMM epilogues
+enum EpiKind : int { EPI_STORE = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_GELU = 3, EPI_QKV = 4 };
+
+struct EpiParams {
+  const float* bias;  // [N] or null
+  void* out;          // EPI_STORE/GELU: T [M, ldo]; EPI_F32/RESID: float [M, ldo]
+  int ldo;
+  // EPI_QKV: columns [0,D) -> q, [D,2D) -> k, [2D,3D) -> v^T, per head.
+  void* q;             // T [clips*n_head, n_tok, head_dim]
+  void* k;             // T [clips*n_head, n_tok, head_dim]
+  void* vt;            // T [clips*n_head, head_dim, ldv]
+  int n_tok, n_head, head_dim, ldv, dmodel;
+  const int* pos_ids;  // optional: grid cell (token id) of each row; else row % n_tok
+  RopeParams rope;
+};
+
+}  // namespace jepa

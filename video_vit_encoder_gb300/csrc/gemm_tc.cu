@@ -1,0 +1,256 @@
+// Tensor-core linear layer for sm_103a: out = epilogue(A W^T + bias).
+//
+// A [M, K] and W [N, K] (both K contiguous, bf16 or fp16) are streamed by TMA
+// into 128B-swizzled shared-memory stages; one thread issues tcgen05.mma
+// (M 128 x N BN x K 16, fp32 accumulator in tensor memory); four epilogue
+// warps drain the accumulator with tcgen05.ld and apply the fused epilogue.
+// The kernel is persistent (one CTA per SM, static tile striding) and keeps
+// two accumulators in tensor memory so the epilogue of one tile overlaps the
+// main loop of the next.
+//
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer and
+// tensor-memory owner, warps 2-5 epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. 32*(w%4)+31).
+#include "epilogue.cuh"
+#include "internal.h"
+
+namespace jepa {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;  // 64 x 16-bit = one 128-byte swizzle row
+constexpr int kThreads = 192;
+
+template <int BN, int STAGES>
+struct GemmSmem {
+  static constexpr uint32_t kABytes = kBM * kBK * 2;
+  static constexpr uint32_t kBBytes = BN * kBK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; a power of two
+  static constexpr size_t kBytes = 1024 /*alignment slack*/ + (size_t)STAGES * kStageBytes + 256;
+};
+
+template <typename T, int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+                   int K, EpiParams ep, int* status) {
+  using S = GemmSmem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * S::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * S::kStageBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;  // [2] accumulator ready for the epilogue
+  uint64_t* tempty = tfull + 2;      // [2] accumulator drained by the epilogue
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_n = (N + BN - 1) / BN;
+  const int num_tiles = ((M + kBM - 1) / kBM) * num_n;
+  const int num_kb = K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, S::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
+        const int tm = tile / num_n, tn = tile - tm * num_n;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            atomicOr(status, DEV_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
+          tma_load_2d(sA + stage * S::kABytes, &tmA, &full[stage], kb * kBK, tm * kBM);
+          tma_load_2d(sB + stage * S::kBBytes, &tmB, &full[stage], kb * kBK, tn * BN);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Every copy this CTA issued must land before it exits: wait (bounded)
+      // for the last min(issued, STAGES) stages.
+      const long pending = issued < STAGES ? issued : STAGES;
+      for (long i = 0; i < pending; ++i) {
+        if (--stage < 0) {
+          stage = STAGES - 1;
+          phase ^= 1;
+        }
+        mbar_wait(&full[stage], phase);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16<T, kBM, BN>();
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++acc) {
+        const int buf = acc & 1;
+        const uint32_t acc_phase = (acc >> 1) & 1;
+        if (!mbar_wait(&tempty[buf], acc_phase ^ 1)) {
+          atomicOr(status, DEV_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase)) {
+            atomicOr(status, DEV_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * S::kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * S::kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            umma_f16_ss(d_tmem, smem_desc_kmajor<128>(a0 + k * 32), smem_desc_kmajor<128>(b0 + k * 32), idesc,
+                        (kb | k) != 0);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[buf]);
+      }
+      // Drain: no MMA may still be running when tensor memory is released.
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++acc) {
+      const int buf = acc & 1;
+      const uint32_t acc_phase = (acc >> 1) & 1;
+      const bool ok = mbar_wait(&tfull[buf], acc_phase);
+      if (__any_sync(0xffffffffu, !ok) || *abort_flag) {
+        if (lane == 0) atomicOr(status, DEV_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int tm = tile / num_n, tn = tile - tm * num_n;
+      const int row = tm * kBM + row_in_tile;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + c * 32, r);
+        tmem_wait_ld();
+        const int col0 = tn * BN + c * 32;
+        if (row < M && col0 < N) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          epilogue_apply<T, EPI, 32>(ep, row, col0, v);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::kTmemCols);
+  }
+}
+
+template <typename T, int BN, int STAGES, int EPI>
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
+                       int* status, cudaStream_t stream, int num_sms) {
+  using S = GemmSmem<BN, STAGES>;
+  auto kern = gemm_tc_kernel<T, BN, STAGES, EPI>;
+  static bool configured = false;  // per instantiation
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  kern<<<grid, kThreads, S::kBytes, stream>>>(ta, tb, M, N, K, ep, status);
+  return cudaGetLastError();
+}
+
+template <typename T, int BN, int STAGES>
+cudaError_t dispatch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
+                         const EpiParams& ep, int* status, cudaStream_t s, int sms) {
+  switch (epi) {
+    case EPI_STORE: return launch_one<T, BN, STAGES, EPI_STORE>(ta, tb, M, N, K, ep, status, s, sms);
+    case EPI_F32: return launch_one<T, BN, STAGES, EPI_F32>(ta, tb, M, N, K, ep, status, s, sms);
+    case EPI_RESID: return launch_one<T, BN, STAGES, EPI_RESID>(ta, tb, M, N, K, ep, status, s, sms);
+    case EPI_GELU: return launch_one<T, BN, STAGES, EPI_GELU>(ta, tb, M, N, K, ep, status, s, sms);
+    case EPI_QKV: return launch_one<T, BN, STAGES, EPI_QKV>(ta, tb, M, N, K, ep, status, s, sms);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t gemm_tc_typed(int epi, const void* A, const void* W, int M, int N, int K, const EpiParams& ep,
+                          int* status, cudaStream_t s, int sms) {
+  const int BN = (N % 256 == 0) ? 256 : 128;
+  CUtensorMap ta, tb;
+  cudaError_t e = make_tmap_2d(&ta, A, sizeof(T), K, M, (size_t)K * sizeof(T), kBK, kBM);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_2d(&tb, W, sizeof(T), K, N, (size_t)K * sizeof(T), kBK, BN);
+  if (e != cudaSuccess) return e;
+  if (BN == 256) return dispatch_epi<T, 256, 4>(epi, ta, tb, M, N, K, ep, status, s, sms);
+  return dispatch_epi<T, 128, 6>(epi, ta, tb, M, N, K, ep, status, s, sms);
+}
+
+}  // namespace
+
+cudaError_t gemm_tc(int dtype, int epi, const void* A, const void* W, int M, int N, int K, const EpiParams& ep,
+                    int* status, cudaStream_t s, int num_sms) {
+  if (dtype == DTYPE_BF16) return gemm_tc_typed<__nv_bfloat16>(epi, A, W, M, N, K, ep, status, s, num_sms);
+  return gemm_tc_typed<__half>(epi, A, W, M, N, K, ep, status, s, num_sms);
+}
+
+}  // namespace jepa

@@ -1,0 +1,51 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace jepa {
+
+// dtype codes of the ABI (jepa_dtype)
+enum : int { DTYPE_F32 = 0, DTYPE_F16 = 1, DTYPE_BF16 = 2 };
+
+// Tensor maps (TMA descriptors), 16-bit elements, 128B or 64B swizzle chosen
+// from the inner box width (128 or 64 bytes).
+cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                         uint32_t box2);
+
+// Linear layers.
+cudaError_t gemm_tc(int dtype, int epi, const void* A, const void* W, int M, int N, int K, const EpiParams& ep,
+                    int* status, cudaStream_t s, int num_sms);
+cudaError_t gemm_simt_f32(int epi, const float* A, const float* W, int M, int N, int K, const EpiParams& ep,
+                          cudaStream_t s);
+
+// Attention: q, k [BH, n, hd]; vt [BH, hd, ldv]; out [B, n, H*hd].
+cudaError_t attention_tc(int dtype, const void* q, const void* k, const void* vt, void* out, int batch, int n_head,
+                         int n_tok, int head_dim, int ldv, float scale, int* status, cudaStream_t s, int num_sms);
+cudaError_t attention_simt(int dtype, const void* q, const void* k, const void* vt, void* out, int batch, int n_head,
+                           int n_tok, int head_dim, int ldv, float scale, cudaStream_t s);
+
+// Element-wise / row-wise kernels.
+cudaError_t unfold_clip_u8(int dtype, const uint8_t* clip, void* out, int batch, int T, int H, int W,
+                           cudaStream_t s);
+cudaError_t unfold_clip_f32(int dtype, const float* clip, void* out, int batch, int T, int H, int W,
+                            cudaStream_t s);
+cudaError_t layernorm(int out_dtype, const float* x, const float* w, const float* b, void* y, int rows, int dim,
+                      float eps, cudaStream_t s);
+cudaError_t mean_pool(const float* x, float* out, int batch, int n_tok, int dim, cudaStream_t s);
+cudaError_t rope_inplace_f32(float* x, int batch, int n_tok, int n_head, int head_dim, const RopeParams& rp,
+                             cudaStream_t s);
+cudaError_t gather_rows_cast(int dtype, const float* src, const int* ids, int n, int dim, void* dst,
+                             cudaStream_t s);
+cudaError_t fill_rows(float* dst, const float* row, int n, int dim, cudaStream_t s);
+cudaError_t add_row_vector(float* x, const float* v, int rows, int dim, cudaStream_t s);
+cudaError_t wait_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace jepa
