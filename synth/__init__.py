@@ -51,12 +51,30 @@ def _stream_key(seed: int, stream: int) -> np.uint64:
     return mix64(base ^ np.uint64(stream & 0xFFFFFFFFFFFFFFFF))[()]
 
 
+def _mix64_inplace(z: np.ndarray, tmp: np.ndarray) -> np.ndarray:
+    # splitmix64 output function on a uint64 array, in place (same values as mix64)
+    np.right_shift(z, np.uint64(30), out=tmp); np.bitwise_xor(z, tmp, out=z); np.multiply(z, _M1, out=z)
+    np.right_shift(z, np.uint64(27), out=tmp); np.bitwise_xor(z, tmp, out=z); np.multiply(z, _M2, out=z)
+    np.right_shift(z, np.uint64(31), out=tmp); np.bitwise_xor(z, tmp, out=z)
+    return z
+
+
+_CHUNK = 1 << 18
+
+
 def draws_u64(seed: int, stream: int, n: int, start: int = 0) -> np.ndarray:
     """Draws ``start .. start+n-1`` of stream ``stream`` under ``seed``."""
     key = _stream_key(seed, stream)
-    idx = np.arange(start + 1, start + n + 1, dtype=np.uint64)
+    out = np.empty(n, dtype=np.uint64)
     with np.errstate(over="ignore"):
-        return mix64(key + idx * GOLDEN)
+        for c0 in range(0, n, _CHUNK):
+            c1 = min(n, c0 + _CHUNK)
+            z = out[c0:c1]
+            z[:] = np.arange(start + c0 + 1, start + c1 + 1, dtype=np.uint64)
+            np.multiply(z, GOLDEN, out=z)
+            np.add(z, key, out=z)
+            _mix64_inplace(z, np.empty_like(z))
+    return out
 
 
 def uniform_u8(seed: int, stream: int, n: int) -> np.ndarray:
@@ -68,12 +86,15 @@ def normal(seed: int, stream: int, n: int, std: float) -> np.ndarray:
     """``n`` samples of N(0, std^2) in float64 (Box-Muller on draw pairs)."""
     m = (n + 1) // 2
     d = draws_u64(seed, stream, 2 * m)
-    u = ((d >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
-    u1, u2 = u[0::2], u[1::2]
-    r = np.sqrt(-2.0 * np.log(u1))
     z = np.empty(2 * m, dtype=np.float64)
-    z[0::2] = r * np.cos(2.0 * np.pi * u2)
-    z[1::2] = r * np.sin(2.0 * np.pi * u2)
+    half = _CHUNK // 2
+    for p0 in range(0, m, half):
+        p1 = min(m, p0 + half)
+        u = ((d[2 * p0:2 * p1] >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
+        r = np.sqrt(-2.0 * np.log(u[0::2]))
+        a = 2.0 * np.pi * u[1::2]
+        z[2 * p0:2 * p1:2] = r * np.cos(a)
+        z[2 * p0 + 1:2 * p1:2] = r * np.sin(a)
     return z[:n] * std
 
 
@@ -157,20 +178,28 @@ def tensor_names_predictor(pc: PredictorConfig):
     return out
 
 
+def _one_tensor(args):
+    idx, (name, shape, kind), seed, storage, stream_base, std = args
+    n = int(np.prod(shape))
+    if kind == "mat":
+        v = round_to_dtype(normal(seed, stream_base + idx, n, std), storage)
+    elif kind == "vec":
+        v = normal(seed, stream_base + idx, n, std).astype(np.float32)
+    elif kind == "zero":
+        v = np.zeros(n, np.float32)
+    else:
+        v = np.ones(n, np.float32)
+    return name, v.reshape(shape)
+
+
 def _materialise(names, seed, storage, stream_base, std=0.02):
-    w = {}
-    for idx, (name, shape, kind) in enumerate(names):
-        n = int(np.prod(shape))
-        if kind == "mat":
-            v = round_to_dtype(normal(seed, stream_base + idx, n, std), storage)
-        elif kind == "vec":
-            v = normal(seed, stream_base + idx, n, std).astype(np.float32)
-        elif kind == "zero":
-            v = np.zeros(n, np.float32)
-        else:
-            v = np.ones(n, np.float32)
-        w[name] = v.reshape(shape)
-    return w
+    # Tensors are independent streams, so they are drawn in parallel threads
+    # (numpy releases the GIL); the values do not depend on the schedule.
+    import concurrent.futures as cf
+    import os
+    jobs = [(i, nk, seed, storage, stream_base, std) for i, nk in enumerate(names)]
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        return dict(ex.map(_one_tensor, jobs))
 
 
 def encoder_weights(cfg: EncoderConfig) -> dict:

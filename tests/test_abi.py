@@ -91,6 +91,7 @@ def test_argument_errors_without_gpu(lib):
     # Host-side validation happens before any CUDA call.
     from video_vit_encoder_gb300._lib import ERR_ARG, ERR_UNSUPPORTED
     assert lib.jepa_layernorm_f32(None, None, None, None, 4, 128, 1e-6, None) == ERR_ARG
+    assert lib.jepa_layernorm_f32(None, None, None, None, 0, 128, 1e-6, None) == 0
     assert lib.jepa_rope3d_f32(C.c_void_p(16), 1, 10, 1, 48, 1, 2, 5, 0, 0, 16, 1e4, None) == ERR_UNSUPPORTED
     assert lib.jepa_rope3d_f32(C.c_void_p(16), 1, 11, 1, 64, 1, 2, 5, 0, 0, 16, 1e4, None) == ERR_ARG
     assert lib.jepa_linear(C.c_void_p(16), C.c_void_p(16), None, C.c_void_p(16), 8, 32, 40, 2, 0, None) == ERR_ARG

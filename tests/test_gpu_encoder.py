@@ -1,0 +1,110 @@
+"""The whole encoder through the C ABI against the oracle.
+
+Small geometries are compared end to end on every token; the fp32 workload
+(single block + patch embed) is compared end to end at its full size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import REL_F32_PATH, assert_close_16bit, assert_close_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def jg():
+    import video_vit_encoder_gb300 as m
+    m.load()
+    return m
+
+
+SMALL = {
+    # 2.1 geometry: interleaved interpolated RoPE, modality vector, hierarchical taps; N = 2*6*8 = 96
+    "b21-bf16": synth.CONFIGS["c5"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=3, n_frames=4,
+                                          height=96, width=128, batch=3, hier_layers=(0, 2)),
+    "b21-f16": synth.CONFIGS["c2"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=3, n_frames=4,
+                                         height=96, width=128, batch=2, hier_layers=(1,)),
+    # V-JEPA 2 geometry, tiled RoPE, head_dim 32, N = 3*5*9 = 135 (ragged against 128-row tiles)
+    "v2-hd32": synth.CONFIGS["c3"].with_(embed_dim=256, n_head=8, ffn_dim=512, n_layer=2, n_frames=6,
+                                         height=80, width=144, batch=2),
+}
+
+
+def _run(jg, cfg, pooled=True, hier=True):
+    w = synth.encoder_weights(cfg)
+    clip = synth.clip_u8(cfg)
+    enc = jg.Encoder(cfg, w)
+    res = enc.encode(torch.from_numpy(clip).cuda(), pooled=pooled, hier=hier)
+    enc.sync()
+    return enc, w, clip, {k: v.cpu().numpy() for k, v in res.items()}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_end_to_end(jg, name):
+    cfg = SMALL[name]
+    enc, w, clip, got = _run(jg, cfg)
+    for b in range(cfg.batch):
+        ref = oracle.encoder_forward(cfg, w, clip[b])
+        assert_close_16bit(got["out"][b], ref["out"], f"{name} clip {b}")
+        np.testing.assert_allclose(got["pooled"][b], ref["pooled"], atol=1e-2 * np.abs(ref["pooled"]).max())
+        for k, tap in enumerate(ref["hier"]):
+            assert_close_16bit(got["hier"][k, b], tap, f"{name} tap {k} clip {b}")
+    enc.close()
+
+
+def test_c1_fp32_end_to_end(jg):
+    cfg = synth.CONFIGS["c1"]
+    enc, w, clip, got = _run(jg, cfg, hier=False)
+    ref = oracle.encoder_forward(cfg, w, clip[0])
+    m = assert_close_f32(got["out"][0], ref["out"], REL_F32_PATH, "c1")
+    print("c1 parity", m)
+    enc.close()
+
+
+def test_embed_then_blocks_equals_encode(jg):
+    cfg = SMALL["b21-bf16"]
+    w = synth.encoder_weights(cfg)
+    clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
+    enc = jg.Encoder(cfg, w)
+    out = enc.encode(clip)["out"]
+    B, T, H, W, _ = clip.shape
+    x = enc.embed(clip)
+    enc.blocks(x, B, T, H, W, 0, 1)
+    enc.blocks(x, B, T, H, W, 1, cfg.n_layer)
+    y = jg.layernorm_f32(x, torch.from_numpy(w["norm.weight"]).cuda(), torch.from_numpy(w["norm.bias"]).cuda(),
+                         cfg.ln_eps)
+    enc.sync()
+    assert torch.equal(y.view_as(out), out)
+    enc.close()
+
+
+def test_encode_host_matches_device(jg):
+    cfg = SMALL["v2-hd32"]
+    w = synth.encoder_weights(cfg)
+    clip = synth.clip_u8(cfg)
+    enc = jg.Encoder(cfg, w)
+    dev = enc.encode(torch.from_numpy(clip).cuda(), pooled=True)
+    enc.sync()
+    hclip = torch.from_numpy(clip).pin_memory()
+    hout = torch.empty(dev["out"].shape, dtype=torch.float32).pin_memory()
+    hpool = torch.empty(dev["pooled"].shape, dtype=torch.float32).pin_memory()
+    enc.encode_host(hclip, hout, hpool)
+    assert torch.equal(hout, dev["out"].cpu())
+    assert torch.equal(hpool, dev["pooled"].cpu())
+    enc.close()
+
+
+def test_batch_independence(jg):
+    # clips are independent: clip 1 of a batch equals the same clip run alone
+    cfg = SMALL["v2-hd32"]
+    w = synth.encoder_weights(cfg)
+    clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
+    enc = jg.Encoder(cfg, w)
+    both = enc.encode(clip)["out"]
+    one = enc.encode(clip[1:2].contiguous())["out"]
+    enc.sync()
+    assert_close_16bit(one[0].cpu().numpy(), both[1].cpu().numpy().astype(np.float64), "batch independence")
+    enc.close()

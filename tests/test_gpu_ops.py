@@ -1,0 +1,142 @@
+"""Single kernels through the C ABI against the oracle, element by element."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import REL_F32_KERNEL, assert_close_16bit, assert_close_f32, metrics
+
+pytestmark = pytest.mark.gpu
+
+TD = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+
+@pytest.fixture(scope="module")
+def jg():
+    import video_vit_encoder_gb300 as m
+    m.load()
+    return m
+
+
+def _dev(a, dtype="f32"):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(TD[dtype]).cuda()
+
+
+def _rounded(rng, shape, dtype, scale=1.0):
+    return synth.round_to_dtype(rng.standard_normal(shape) * scale, dtype).astype(np.float64)
+
+
+def test_wait_timeout_reports_and_context_survives(jg):
+    from video_vit_encoder_gb300._lib import ERR_DEVICE_TIMEOUT
+    assert jg.selftest_wait_timeout(200) == ERR_DEVICE_TIMEOUT
+    x = torch.randn(8, 128, device="cuda")
+    y = jg.layernorm_f32(x, torch.ones(128, device="cuda"), torch.zeros(128, device="cuda"), 1e-6)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y).all()
+    jg.ops_sync()
+
+
+@pytest.mark.parametrize("rows,dim", [(1000, 768), (37, 1024), (5, 384), (0, 128)])
+def test_layernorm_f32(jg, rows, dim):
+    rng = np.random.default_rng(rows + dim)
+    x = rng.standard_normal((rows, dim)) * 3 + rng.standard_normal((rows, 1)) * 2
+    w, b = rng.standard_normal(dim), rng.standard_normal(dim)
+    x32, w32, b32 = (np.float32(t) for t in (x, w, b))
+    y = jg.layernorm_f32(_dev(x32), _dev(w32), _dev(b32), 1e-6).cpu().numpy()
+    if rows == 0:
+        return
+    ref = oracle.layer_norm(x32.astype(np.float64), w32, b32, 1e-6)
+    m = metrics(y, ref)
+    assert m["rel_max"] <= REL_F32_KERNEL, m
+
+
+@pytest.mark.parametrize("hd,layout,interp,grid", [
+    (64, "tiled", False, (8, 16, 16)), (64, "interleaved", True, (4, 24, 24)),
+    (32, "tiled", False, (32, 4, 4)), (64, "interleaved", True, (3, 20, 7))])
+def test_rope3d_f32(jg, hd, layout, interp, grid):
+    gt, gh, gw = grid
+    N, H, B = gt * gh * gw, 3, 2
+    rng = np.random.default_rng(hd + N)
+    x = np.float32(rng.standard_normal((B, N, H * hd)))
+    t = _dev(x)
+    jg.rope3d_f32(t, grid, H, hd, layout, interp)
+    got = t.cpu().numpy().reshape(B, N, H, hd)
+    pos = oracle.token_positions(gt, gh, gw, interp, 16)
+    COS, SIN = oracle.rope_tables(pos, hd, layout)
+    ref = oracle.apply_rope(x.astype(np.float64).reshape(B, N, H, hd).transpose(0, 2, 1, 3), COS, SIN)
+    m = metrics(got, ref.transpose(0, 2, 1, 3))
+    assert m["rel_max"] <= REL_F32_KERNEL, m
+
+
+def _linear_ref(A, W, b, epi, resid=None):
+    acc = A @ W.T + b
+    if epi == 2:
+        return resid + acc
+    if epi == 3:
+        return oracle.gelu_erf(acc)
+    return acc
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3])
+@pytest.mark.parametrize("M,N,K", [(300, 256, 1536), (128, 384, 384), (1000, 768, 1024), (64, 1152, 128)])
+def test_linear(jg, dtype, epi, M, N, K):
+    rng = np.random.default_rng(M + N + K + epi)
+    A = _rounded(rng, (M, K), dtype)
+    W = _rounded(rng, (N, K), dtype, 0.02)
+    b = rng.standard_normal(N).astype(np.float32).astype(np.float64) * 0.1
+    resid = rng.standard_normal((M, N)).astype(np.float32).astype(np.float64)
+    out = _dev(resid) if epi == 2 else None
+    got = jg.linear(_dev(A, dtype), _dev(W, dtype), _dev(b), epi, out=out)
+    got = got.float().cpu().numpy()
+    ref = _linear_ref(A, W, b, epi, resid)
+    if dtype == "f32" or epi in (1, 2):
+        m = metrics(got, ref)
+        assert m["rel_max"] <= (1e-5 if dtype == "f32" else 1e-4), (dtype, epi, m)
+    else:
+        assert_close_16bit(got, ref, f"linear {dtype} epi {epi}")
+
+
+def _attn_inputs(rng, B, H, N, hd, dtype, logit_std):
+    # q k^T / sqrt(hd) has std ~ sq*sk*sqrt(hd)/sqrt(hd) = sq*sk
+    s = math.sqrt(logit_std)
+    q = _rounded(rng, (B * H, N, hd), dtype, s)
+    k = _rounded(rng, (B * H, N, hd), dtype, s)
+    v = _rounded(rng, (B * H, N, hd), dtype)
+    return q, k, v
+
+
+def _run_attn(jg, q, k, v, B, H, N, hd, dtype):
+    ldv = (N + 7) // 8 * 8
+    vt = np.zeros((B * H, hd, ldv))
+    vt[:, :, :N] = v.transpose(0, 2, 1)
+    out = jg.attention(_dev(q, dtype), _dev(k, dtype), _dev(vt, dtype), B, H, N, hd)
+    jg.ops_sync()
+    return out.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("hd", [64, 32])
+@pytest.mark.parametrize("N,logit_std", [(200, 1.0), (384, 4.0), (1000, 1.0), (128, 0.3)])
+def test_attention_tc(jg, dtype, hd, N, logit_std):
+    B, H = 2, 3
+    rng = np.random.default_rng(N + hd)
+    q, k, v = _attn_inputs(rng, B, H, N, hd, dtype, logit_std)
+    if logit_std > 2:   # a planted large logit on a few rows
+        k[:, 7] = synth.round_to_dtype(q[:, 3] * 3, dtype)
+    got = _run_attn(jg, q, k, v, B, H, N, hd, dtype)
+    ref = oracle.attention_heads(q, k, v).reshape(B, H, N, hd).transpose(0, 2, 1, 3).reshape(B, N, H * hd)
+    assert_close_16bit(got, ref, f"attention {dtype} hd{hd} N{N}")
+
+
+@pytest.mark.parametrize("hd,N", [(64, 130), (32, 77)])
+def test_attention_f32(jg, hd, N):
+    B, H = 1, 2
+    rng = np.random.default_rng(N)
+    q, k, v = _attn_inputs(rng, B, H, N, hd, "f32", 2.0)
+    got = _run_attn(jg, q, k, v, B, H, N, hd, "f32")
+    ref = oracle.attention_heads(q, k, v).reshape(B, H, N, hd).transpose(0, 2, 1, 3).reshape(B, N, H * hd)
+    assert_close_f32(got, ref, 1e-5)

@@ -50,6 +50,7 @@ jepa_status fail(jepa_status st, const char* fmt, ...) {
   } while (0)
 
 size_t dtype_size(int dt) { return dt == DTYPE_F32 ? 4 : 2; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ----------------------------------------------------------------------------- blob
@@ -690,6 +691,7 @@ jepa_status jepa_encoder_embed(jepa_encoder* enc, const void* clip, int clip_for
   Geom g;
   JEPA_TRY(check_clip(enc, batch, n_frames, height, width, g));
   if (clip == nullptr || x_out == nullptr) return fail(JEPA_ERR_ARG, "clip and x_out must be device buffers");
+  if (!aligned16(clip) || !aligned16(x_out)) return fail(JEPA_ERR_ARG, "device buffers must be 16-byte aligned");
   if (clip_format != JEPA_CLIP_U8_THWC && clip_format != JEPA_CLIP_F32_CTHW)
     return fail(JEPA_ERR_ARG, "clip_format %d", clip_format);
   cudaStream_t s = (cudaStream_t)stream;
@@ -703,7 +705,7 @@ jepa_status jepa_encoder_blocks(jepa_encoder* enc, float* x, int batch, int n_fr
                                 int layer_begin, int layer_end, void* stream) {
   Geom g;
   JEPA_TRY(check_clip(enc, batch, n_frames, height, width, g));
-  if (x == nullptr) return fail(JEPA_ERR_ARG, "x must be a device buffer");
+  if (x == nullptr || !aligned16(x)) return fail(JEPA_ERR_ARG, "x must be a 16-byte aligned device buffer");
   if (layer_begin < 0 || layer_end > enc->p.n_layer || layer_begin > layer_end)
     return fail(JEPA_ERR_ARG, "layer range [%d, %d) outside [0, %d)", layer_begin, layer_end, enc->p.n_layer);
   cudaStream_t s = (cudaStream_t)stream;
@@ -723,6 +725,8 @@ jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_format, in
   Geom g;
   JEPA_TRY(check_clip(enc, batch, n_frames, height, width, g));
   if (clip == nullptr || out_tokens == nullptr) return fail(JEPA_ERR_ARG, "clip and out_tokens are required");
+  if (!aligned16(clip) || !aligned16(out_tokens) || !aligned16(out_pooled) || !aligned16(out_hier))
+    return fail(JEPA_ERR_ARG, "device buffers must be 16-byte aligned");
   if (clip_format != JEPA_CLIP_U8_THWC && clip_format != JEPA_CLIP_F32_CTHW)
     return fail(JEPA_ERR_ARG, "clip_format %d", clip_format);
   cudaStream_t s = (cudaStream_t)stream;
@@ -892,6 +896,7 @@ jepa_status jepa_predict(jepa_predictor* pr, const float* enc_tokens, int n_toke
   if (pr == nullptr) return fail(JEPA_ERR_ARG, "predictor handle is NULL");
   if (enc_tokens == nullptr || ids_ctx == nullptr || ids_tgt == nullptr || out == nullptr)
     return fail(JEPA_ERR_ARG, "device buffers are required");
+  if (!aligned16(enc_tokens) || !aligned16(out)) return fail(JEPA_ERR_ARG, "buffers must be 16-byte aligned");
   if (n_ctx < 1 || n_tgt < 1 || n_tokens < 1) return fail(JEPA_ERR_ARG, "n_ctx, n_tgt and n_tokens must be >= 1");
   if (grid_t < 1 || grid_h < 1 || grid_w < 1 || (long long)grid_t * grid_h * grid_w != n_tokens)
     return fail(JEPA_ERR_ARG, "grid %dx%dx%d does not hold %d tokens", grid_t, grid_h, grid_w, n_tokens);
@@ -965,16 +970,18 @@ jepa_status jepa_predictor_sync(jepa_predictor* pr, void* stream) {
 // ============================================================================= single operations
 jepa_status jepa_layernorm_f32(const float* x, const float* w, const float* b, float* y, int rows, int dim, float eps,
                                void* stream) {
-  if (!x || !w || !b || !y) return fail(JEPA_ERR_ARG, "NULL buffer");
   if (rows < 0 || dim <= 0 || dim % 128 != 0 || dim > 4096)
     return fail(JEPA_ERR_ARG, "rows %d / dim %d (dim a multiple of 128, <= 4096)", rows, dim);
+  if (rows == 0) return JEPA_OK;
+  if (!x || !w || !b || !y) return fail(JEPA_ERR_ARG, "NULL buffer");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(y)) return fail(JEPA_ERR_ARG, "buffers must be 16-byte aligned");
   if (!(eps > 0.f)) return fail(JEPA_ERR_ARG, "eps must be > 0");
   return cuda_status(layernorm(DTYPE_F32, x, w, b, y, rows, dim, eps, (cudaStream_t)stream), "layernorm");
 }
 
 jepa_status jepa_rope3d_f32(float* x, int batch, int n_tokens, int n_head, int head_dim, int grid_t, int grid_h,
                             int grid_w, int layout, int interpolate, int ref_grid, float theta, void* stream) {
-  if (!x) return fail(JEPA_ERR_ARG, "NULL buffer");
+  if (!x || !aligned16(x)) return fail(JEPA_ERR_ARG, "x must be a 16-byte aligned buffer");
   if (head_dim != 32 && head_dim != 64) return fail(JEPA_ERR_UNSUPPORTED, "head_dim %d (32 or 64)", head_dim);
   if (batch < 0 || n_head < 1 || grid_t < 1 || grid_h < 1 || grid_w < 1 ||
       (long long)grid_t * grid_h * grid_w != n_tokens)
@@ -993,6 +1000,7 @@ jepa_status jepa_rope3d_f32(float* x, int batch, int n_tokens, int n_head, int h
 jepa_status jepa_attention(const void* q, const void* k, const void* vt, void* out, int dtype, int batch, int n_head,
                            int n_tokens, int head_dim, int ldv, float scale, void* stream) {
   if (!q || !k || !vt || !out) return fail(JEPA_ERR_ARG, "NULL buffer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(out)) return fail(JEPA_ERR_ARG, "buffers must be 16-byte aligned");
   if (dtype < 0 || dtype > 2) return fail(JEPA_ERR_ARG, "dtype %d", dtype);
   if (head_dim != 32 && head_dim != 64) return fail(JEPA_ERR_UNSUPPORTED, "head_dim %d (32 or 64)", head_dim);
   if (batch < 1 || n_head < 1 || n_tokens < 1) return fail(JEPA_ERR_ARG, "batch, n_head, n_tokens must be >= 1");
@@ -1014,6 +1022,7 @@ jepa_status jepa_attention(const void* q, const void* k, const void* vt, void* o
 jepa_status jepa_linear(const void* A, const void* W, const float* bias, void* out, int M, int N, int K, int dtype,
                         int epilogue, void* stream) {
   if (!A || !W || !out) return fail(JEPA_ERR_ARG, "NULL buffer");
+  if (!aligned16(A) || !aligned16(W) || !aligned16(out) || !aligned16(bias)) return fail(JEPA_ERR_ARG, "buffers must be 16-byte aligned");
   if (dtype < 0 || dtype > 2) return fail(JEPA_ERR_ARG, "dtype %d", dtype);
   if (epilogue < 0 || epilogue > 3) return fail(JEPA_ERR_ARG, "epilogue %d", epilogue);
   if (M < 0 || N <= 0 || K <= 0) return fail(JEPA_ERR_ARG, "M %d N %d K %d", M, N, K);
