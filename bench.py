@@ -1,0 +1,337 @@
+"""Throughput of the V-JEPA 2 ViT-L/16 encoder forward on GB300.
+
+Workload: ViT-L/16 (D 1024, 24 layers, 16 heads, FFN 4096), bf16 weights and
+activations with fp32 accumulation and fp32 residual stream, tiled 3-D RoPE,
+clips of 16 frames x 256 x 256 (2048 tokens each), batch 8 per GPU.  Weights
+N(0, 0.02) and uniform uint8 clips from the seeded generator (synthetic: the
+pages' real clips and checkpoints are not available).
+
+One step = one jepa_encode call over the batch (patch embed, 24 blocks, final
+LayerNorm), inputs already resident in HBM.  The L2 cache (129 MB) is flushed
+between timed steps by writing a 256 MB buffer outside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own replica (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "encoder tokens/sec (ViT-L/16, 16f 256px, bf16) and % of bf16 tensor peak"
+UNIT = "tokens/s"
+WORKLOAD = "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 16f x 256x256 (2048 tokens/clip), batch 8 per GPU"
+CLASSES = ["patch_embed", "layernorm", "qkv_gemm", "attention", "out_proj_gemm", "ffn_up_gemm", "ffn_down_gemm",
+           "other"]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"bf16_burst": d["bf16_tflops"], "bf16_sustained": d["bf16_tflops_sustained"],
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def flops_per_clip(cfg, n_tok):
+    """Algorithmic FLOPs of one clip: per token L*(24 D^2 + 4 N D) + 2*1536*D."""
+    D, L, F = cfg.embed_dim, cfg.n_layer, cfg.ffn_dim
+    per_tok_layer = 2 * (3 * D * D + D * D + 2 * D * F) + 4 * n_tok * D
+    return n_tok * (L * per_tok_layer + 2 * 1536 * D)
+
+
+def class_flops_per_launch(cfg, batch, n_tok):
+    D, F, H = cfg.embed_dim, cfg.ffn_dim, cfg.n_head
+    M = batch * n_tok
+    return {"patch_embed": 2 * M * 1536 * D, "qkv_gemm": 2 * M * D * 3 * D, "attention": 4 * batch * H * n_tok * n_tok * (D // H),
+            "out_proj_gemm": 2 * M * D * D, "ffn_up_gemm": 2 * M * D * F, "ffn_down_gemm": 2 * M * F * D}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_for(kernel_class, launch_key):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_class)
+    if not e or e.get("launch") != launch_key:
+        return None
+    if e.get("source_sha") != _source_sha(e.get("sources", [])):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(cfg, weights, clip, blocks=2):
+    """The oracle, as it stands, on the host cores: one clip, patch embed + a
+    few blocks timed; the full-clip time is the embed time plus the mean block
+    time x n_layer (plus the final norm)."""
+    import numpy as np
+    import oracle
+    T, H, W, _ = clip.shape
+    t0 = time.perf_counter()
+    x = oracle.encoder_embed(cfg, weights, clip)
+    t_embed = time.perf_counter() - t0
+    COS, SIN = oracle.encoder_rope(cfg, T, H, W)
+    t0 = time.perf_counter()
+    for i in range(blocks):
+        x = oracle.block_forward(x, weights, i, cfg.n_head, cfg.ln_eps, COS, SIN)
+    t_blocks = (time.perf_counter() - t0) / blocks
+    t0 = time.perf_counter()
+    oracle.layer_norm(x, weights["norm.weight"], weights["norm.bias"], cfg.ln_eps)
+    t_norm = time.perf_counter() - t0
+    est = t_embed + cfg.n_layer * t_blocks + t_norm
+    n_tok = x.shape[0]
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=os.cpu_count())
+    except Exception:
+        cores = os.cpu_count()
+    return {"value": n_tok / est, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"1 clip: patch embed + {blocks} of {cfg.n_layer} blocks + final norm timed in float64; "
+                      f"clip time = embed + {cfg.n_layer} x mean block + norm = {est:.2f} s",
+            "seconds_per_clip": est}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, timed on the host cores."""
+    import numpy as np
+    import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cfg = synth.CONFIGS["c3"]
+    w = synth.encoder_weights(cfg)
+    clip = synth.clip_u8(cfg, batch=1)[0]
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(cfg, w, clip, blocks=1)
+        if i >= args.warmup:
+            vals.append(r)
+    v = statistics.median(x["value"] for x in vals)
+    sec = statistics.median(x["seconds_per_clip"] for x in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1000.0 * cfg.batch,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": cfg.batch, "seq_len": 2048, "parallelism": "none",
+                       "note": "CPU oracle; one clip sampled per step, scaled to the batch"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": vals[0]["cores"], "kind": "oracle",
+                             "sample": vals[0]["sample"].replace(" + 1 of", " + 1 of")},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+
+    import synth
+    import video_vit_encoder_gb300 as jg
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    cfg = synth.CONFIGS["c3"]
+    B = cfg.batch
+    n_tok = synth.tokens_per_clip(cfg)
+    weights = synth.encoder_weights(cfg)
+    # each rank encodes its own clips (clip streams rank*B .. rank*B+B-1)
+    clip_np = synth.clip_u8(cfg, batch=B, first_clip=rank * B)
+    enc = jg.Encoder(cfg, weights, device=local)
+    clip = torch.from_numpy(clip_np).cuda()
+    out = torch.empty((B, n_tok, cfg.embed_dim), dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        enc.encode(clip, out=out)
+    enc.sync()
+    enc.profile(reset=True)
+    enc.set_profiling(True)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.fill_(float(i))                     # L2 flush, outside the timed region
+            starts[i].record(stream)
+            enc.encode(clip, out=out)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    enc.sync()
+    if dist:
+        dist.barrier()
+    enc.set_profiling(False)
+    prof = enc.profile(reset=True)
+    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    tokens = world * B * n_tok * args.steps
+    value = tokens / (total_ms / 1e3)
+    fl_step = B * flops_per_clip(cfg, n_tok)
+    peaks = _peaks()
+    tflops = fl_step / (ms_step / 1e3) / 1e12
+
+    # dominant kernel class and its roofline
+    dom = max((k for k in prof if k in class_flops_per_launch(cfg, B, n_tok)), key=lambda k: prof[k][0])
+    t_ms, launches = prof[dom]
+    avg_ms = t_ms / max(launches, 1)
+    fl = class_flops_per_launch(cfg, B, n_tok)[dom]
+    achieved = fl / (avg_ms / 1e3) / 1e12
+    launch_key = f"B{B} N{n_tok} D{cfg.embed_dim}"
+    roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"],
+            "traffic": _traffic_for(dom, launch_key),
+            "peak_note": f"{peaks['source']} sustained bf16 (kernel timed inside a long step)",
+            "avg_launch_ms": avg_ms, "flops_per_launch": fl}
+    kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps} for k, v in prof.items()}
+    gpu_launches = int(sum(v[1] for v in prof.values())) + args.steps  # + the unfold kernel inside patch_embed
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    hclip = torch.from_numpy(clip_np).pin_memory()
+    hout = torch.empty((B, n_tok, cfg.embed_dim), dtype=torch.float32).pin_memory()
+    enc.encode_host(hclip, hout)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        enc.encode_host(hclip, hout)
+    e2e_s = (time.perf_counter() - t0) / args.e2e_steps
+    e2e_val = B * n_tok / e2e_s
+    if dist:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_val = world * B * n_tok / float(t.item())
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights, uniform uint8 clips)",
+        "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": n_tok,
+                   "parallelism": f"replicas x{world}" if world > 1 else "none",
+                   "l2": "flushed between timed steps (256 MB write outside the timed region)"},
+        "clips_per_s": value / n_tok,
+        "tflops": tflops, "pct_bf16_peak": {"burst": tflops / peaks["bf16_burst"],
+                                            "sustained": tflops / peaks["bf16_sustained"], "source": peaks["source"]},
+        "roofline": roof,
+        "kernels": kernels,
+        "gpu_launches": gpu_launches,
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(hclip.numel()),
+                "d2h_bytes_per_step": int(hout.numel() * 4), "api": "jepa_encode_host (pinned host buffers)"},
+        "clocks": clocks.summary(),
+        "context_baseline": {"value": 2048 / 0.0465, "unit": UNIT,
+                             "what": "pages' ggml-CUDA f16 ViT-L/16 16f 256px, batch 1, RTX 4500 Ada (context only)"},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, weights, clip_np[0])
+        line["cpu_baseline"].pop("seconds_per_clip", None)
+    enc.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

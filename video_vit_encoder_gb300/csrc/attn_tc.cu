@@ -197,7 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const bool w_ok = mbar_wait(&s_full[j & 1], (j >> 1) & 1);
-      if (__any_sync(0xffffffffu, !w_ok) || *abort_flag) {
+      // tcgen05.ld/st are warp-collective: every decision that guards them is warp-uniform.
+      if (__any_sync(0xffffffffu, !w_ok || *abort_flag)) {
         ok = false;
         break;
       }
@@ -220,17 +221,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mx = s[0];
 #pragma unroll
       for (int i = 1; i < kBKV; ++i) mx = fmaxf(mx, s[i]);
-      if (j == 0) {
-        m = mx;
-      } else if (mx > m + 8.0f) {
-        // Move the running max: O and l are rescaled by 2^(m_old - m_new).
-        const float corr = exp2f(m - mx);
+      if (j == 0) m = mx;
+      // Move the running max of the whole warp's rows when any of them grew by
+      // more than 2^8: O and l are rescaled by 2^(m_old - m_new) (1 for rows
+      // whose max did not grow).
+      if (__any_sync(0xffffffffu, j > 0 && mx > m + 8.0f)) {
+        const float m_new = fmaxf(m, mx);
+        const float corr = exp2f(m - m_new);
         const int jp = j - 1;
-        const bool pv_ok = mbar_wait(&pv_done[jp & 1], (jp >> 1) & 1);
-        if (!pv_ok) {
-          ok = false;
-          // fall through to arrive so the MMA warp is not left waiting forever
-        }
+        if (!mbar_wait(&pv_done[jp & 1], (jp >> 1) & 1)) ok = false;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
@@ -243,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         l *= corr;
-        m = mx;
+        m = m_new;
       }
       // P_j may overwrite its buffer only after PV_{j-2} has read it.
       if (j >= 2) {

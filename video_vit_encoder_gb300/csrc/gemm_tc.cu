@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = acc & 1;
       const uint32_t acc_phase = (acc >> 1) & 1;
       const bool ok = mbar_wait(&tfull[buf], acc_phase);
-      if (__any_sync(0xffffffffu, !ok) || *abort_flag) {
+      // tcgen05.ld is warp-collective: the stop decision is warp-uniform.
+      if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
         if (lane == 0) atomicOr(status, DEV_TIMEOUT);
         *abort_flag = 1;
         break;
