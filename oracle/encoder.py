@@ -67,14 +67,11 @@ def patch_embed(x: np.ndarray, weight: np.ndarray, bias: np.ndarray,
     D = weight.shape[0]
     K = np.asarray(weight, F64).reshape(D, C, tubelet, patch, patch)
     gt, gh, gw = T // tubelet, H // patch, W // patch
-    out = np.zeros((gt, gh, gw, D), F64)
-    for dt in range(tubelet):
-        for y in range(patch):
-            for xx in range(patch):
-                # samples x[c, tubelet*t+dt, patch*i+y, patch*j+xx] for every cell
-                tap = x[:, dt:gt * tubelet:tubelet, y:gh * patch:patch, xx:gw * patch:patch]
-                out += np.einsum("dc,cthw->thwd", K[:, :, dt, y, xx], tap)
-    out += np.asarray(bias, F64)
+    # x[c, tubelet*t + dt, patch*i + y, patch*j + xx] viewed as [c, t, dt, i, y, j, xx]
+    xv = x[:, :gt * tubelet, :gh * patch, :gw * patch].reshape(C, gt, tubelet, gh, patch, gw, patch)
+    # the sum over every kernel tap (c, dt, y, xx) at every output cell (t, i, j)
+    out = np.einsum("dcpyx,ctpiyjx->tijd", K, xv, optimize=True)
+    out = out + np.asarray(bias, F64)
     return out.reshape(gt * gh * gw, D)
 
 
@@ -183,11 +180,14 @@ def attention_heads(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
     K/V dtype").  Softmax is max-subtracted, exponentiated and normalised.
     """
     hd = q.shape[-1]
-    s = np.matmul(q, np.swapaxes(k, -1, -2)) / math.sqrt(hd)
-    s = s - s.max(axis=-1, keepdims=True)
-    p = np.exp(s)
-    p = p / p.sum(axis=-1, keepdims=True)
-    return np.matmul(p, v)
+    out = np.empty(q.shape[:-1] + (v.shape[-1],), F64)
+    for h in np.ndindex(q.shape[:-2]):        # one head at a time
+        s = (q[h] @ k[h].T) / math.sqrt(hd)
+        s = s - s.max(axis=-1, keepdims=True)
+        p = np.exp(s)
+        p = p / p.sum(axis=-1, keepdims=True)
+        out[h] = p @ v[h]
+    return out
 
 
 def _linear(x, w, b):
