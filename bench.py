@@ -322,7 +322,7 @@ def main():
                              "what": "pages' ggml-CUDA f16 ViT-L/16 16f 256px, batch 1, RTX 4500 Ada (context only)"},
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, weights, clip_np[0])
+        line["cpu_baseline"] = cpu_baseline(cfg, weights, clip_np[0], blocks=4)
         line["cpu_baseline"].pop("seconds_per_clip", None)
     enc.close()
     if rank == 0:

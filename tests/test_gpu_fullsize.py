@@ -1,0 +1,157 @@
+"""Full-size workloads on the GPU against the oracle.
+
+At these sizes the oracle checks what it can compute in seconds:
+  * c3 (ViT-L/16, 8 clips of 16x256x256, the benchmark's launch) - clip 0 end
+    to end on every token, clip 7 block by block on sampled rows;
+  * c2, c4, c5 - block by block on sampled rows (each block recomputed by the
+    oracle from the GPU's own input residual), the final norm and the
+    hierarchical taps on sampled rows, and the c4 predictor end to end.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import assert_close_16bit, metrics
+
+pytestmark = pytest.mark.gpu
+
+_W = {}
+
+
+def _weights(name):
+    if name not in _W:
+        _W[name] = synth.encoder_weights(synth.CONFIGS[name])
+    return _W[name]
+
+
+@pytest.fixture(scope="module")
+def jg():
+    import video_vit_encoder_gb300 as m
+    m.load()
+    return m
+
+
+def _sample_rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.concatenate([[0, n - 1], rng.choice(np.arange(1, n - 1), size=k - 2, replace=False)])
+    return np.sort(rows)
+
+
+def _check_blocks(enc, cfg, w, clip_t, clip_idx, n_rows, seed, stats):
+    """Runs the GPU one block at a time; after each block compares sampled rows
+    of clip `clip_idx` with the oracle's block applied to the GPU's input."""
+    B, T, H, W, _ = clip_t.shape
+    N = synth.tokens_per_clip(cfg)
+    D = cfg.embed_dim
+    x = enc.embed(clip_t)
+    enc.sync()
+    COS, SIN = oracle.encoder_rope(cfg, T, H, W)
+    ref0 = oracle.encoder_embed(cfg, w, clip_t[clip_idx].cpu().numpy())
+    rows = _sample_rows(N, n_rows, seed)
+    got0 = x.view(B, N, D)[clip_idx].cpu().numpy().astype(np.float64)
+    m = metrics(got0[rows], ref0[rows])
+    assert m["rel_max"] <= 1e-2 and m["cos_worst"] >= 0.9999, ("patch embed", m)
+    for l in range(cfg.n_layer):
+        x_in = x.view(B, N, D)[clip_idx].cpu().numpy().astype(np.float64)
+        enc.blocks(x, B, T, H, W, l, l + 1)
+        enc.sync()
+        got = x.view(B, N, D)[clip_idx].cpu().numpy().astype(np.float64)
+        ref = oracle.block_forward_rows(x_in, w, l, cfg.n_head, cfg.ln_eps, COS, SIN, rows)
+        assert_close_16bit(got[rows], ref, f"{cfg.name} block {l} output")
+        md = metrics(got[rows] - x_in[rows], ref - x_in[rows])   # the block's own contribution
+        stats.append((l, md))
+        assert md["cos_mean"] >= 0.9999 and md["cos_worst"] >= 0.999 and md["rel_max"] <= 2e-2, (l, md)
+    return x, rows
+
+
+def test_c3_clip0_end_to_end(jg):
+    cfg = synth.CONFIGS["c3"]
+    w = _weights("c3")
+    clip = synth.clip_u8(cfg)
+    enc = jg.Encoder(cfg, w)
+    res = enc.encode(torch.from_numpy(clip).cuda(), pooled=True)
+    enc.sync()
+    out = res["out"].cpu().numpy()
+    ref = oracle.encoder_forward(cfg, w, clip[0])
+    m = assert_close_16bit(out[0], ref["out"], "c3 clip 0")
+    print("c3 clip 0 end to end:", m)
+    np.testing.assert_allclose(res["pooled"][0].cpu().numpy(), ref["pooled"], atol=1e-2 * np.abs(ref["pooled"]).max())
+    enc.close()
+
+
+def test_c3_clip7_blocks(jg):
+    cfg = synth.CONFIGS["c3"]
+    w = _weights("c3")
+    clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
+    enc = jg.Encoder(cfg, w)
+    stats = []
+    x, rows = _check_blocks(enc, cfg, w, clip, 7, 48, 3, stats)
+    print("c3 clip 7 per-block delta worst cos:", min(s[1]["cos_worst"] for s in stats),
+          "max rel:", max(s[1]["rel_max"] for s in stats))
+    enc.close()
+
+
+def test_c2_blocks_and_final(jg):
+    cfg = synth.CONFIGS["c2"]
+    w = _weights("c2")
+    clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
+    enc = jg.Encoder(cfg, w)
+    stats = []
+    x, rows = _check_blocks(enc, cfg, w, clip, 0, 48, 5, stats)
+    out = enc.encode(clip)["out"]
+    enc.sync()
+    xr = x.cpu().numpy().astype(np.float64)[rows]
+    ref = oracle.layer_norm(xr, w["norm.weight"], w["norm.bias"], cfg.ln_eps)
+    assert_close_16bit(out[0].cpu().numpy()[rows], ref, "c2 final norm")
+    enc.close()
+
+
+def test_c5_blocks_taps_final(jg):
+    cfg = synth.CONFIGS["c5"]
+    w = _weights("c5")
+    clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
+    enc = jg.Encoder(cfg, w)
+    res = enc.encode(clip, hier=True)
+    enc.sync()
+    B, T, H, W, _ = clip.shape
+    N, D = synth.tokens_per_clip(cfg), cfg.embed_dim
+    # taps and output from the GPU's own residual after each tapped block
+    stats = []
+    x, rows = _check_blocks(enc, cfg, w, clip, 0, 32, 9, stats)
+    x_l = enc.embed(clip)
+    done = 0
+    for k, layer in enumerate(cfg.hier_layers):
+        enc.blocks(x_l, B, T, H, W, done, layer + 1)
+        done = layer + 1
+        enc.sync()
+        xr = x_l.view(N, D).cpu().numpy().astype(np.float64)[rows]
+        ref = oracle.layer_norm(xr, w[f"hier_norm.{k}.weight"], w[f"hier_norm.{k}.bias"], cfg.ln_eps)
+        assert_close_16bit(res["hier"][k, 0].cpu().numpy()[rows], ref, f"c5 tap {k}")
+    ref = oracle.layer_norm(x_l.view(N, D).cpu().numpy().astype(np.float64)[rows], w["norm.weight"], w["norm.bias"],
+                            cfg.ln_eps)
+    assert_close_16bit(res["out"][0].cpu().numpy()[rows], ref, "c5 final norm")
+    enc.close()
+
+
+def test_c4_encoder_blocks_and_predictor(jg):
+    cfg = synth.CONFIGS["c4"]
+    w = _weights("c4")
+    clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
+    enc = jg.Encoder(cfg, w)
+    stats = []
+    _check_blocks(enc, cfg, w, clip, 0, 32, 11, stats)
+    tokens = enc.encode(clip)["out"][0].contiguous()
+    enc.sync()
+    enc.close()
+    pc = cfg.predictor
+    pw = synth.predictor_weights(cfg)
+    ctx, tgt = synth.context_target_split(cfg)
+    pred = jg.Predictor(pc, pw, cfg.dtype)
+    out = pred.predict(tokens, torch.from_numpy(ctx).cuda(), torch.from_numpy(tgt).cuda(), cfg.grid())
+    pred.sync()
+    ref = oracle.predictor_forward(pc, pw, tokens.cpu().numpy().astype(np.float64), ctx, tgt, cfg.grid())
+    m = assert_close_16bit(out.cpu().numpy(), ref, "c4 predictor")
+    print("c4 predictor:", m)
+    pred.close()
