@@ -237,6 +237,32 @@ JEPA_API jepa_status jepa_ops_sync(void* stream);
  * the expired wait (the expected outcome); the context stays usable. */
 JEPA_API jepa_status jepa_selftest_wait_timeout(int timeout_us, void* stream);
 
+/* Patch embedding that allocates no device memory.  The paper has no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc themselves, such as a host application or inference server that
+ * owns all device memory through its own pool, or a latency-critical loop that
+ * cannot afford cudaMalloc's device-wide synchronisation or its failure under
+ * memory pressure.  It computes what jepa_encoder_embed computes, without an
+ * encoder handle:
+ *   clip:   device uint8 [batch, n_frames, height, width, 3] (THWC);
+ *   weight: device dtype [embed_dim, 1536] (the patch-embed matrix, feature
+ *           order C,T,H,W); bias: device float [embed_dim] or NULL;
+ *   x_out:  device float [batch*N, embed_dim], N = (n_frames/2)(height/16)(width/16);
+ *   status: optional device int the kernels OR 1 into if a barrier wait
+ *           expired (read it after synchronising); NULL uses a library word
+ *           that is not reported;
+ *   dtype:  JEPA_DT_BF16 or JEPA_DT_F16.
+ * The unfolded patches live in a static device array of 4096 token rows x
+ * 1536 16-bit values (12 MiB) that every GPU loading the library holds until
+ * the process exits; batch*N above 4096 is rejected with JEPA_ERR_ARG before
+ * anything is launched.  All calls on a device share that array: calls whose
+ * GPU work overlaps race on it.  The first call on each device (with that
+ * device current) looks up the array's device address; make that first call
+ * before any stream capture.  Nothing in this call allocates. */
+JEPA_API jepa_status jepa_patch_embed_static(const void* clip, const void* weight, const float* bias, float* x_out,
+                                             int* status, int batch, int n_frames, int height, int width,
+                                             int embed_dim, int dtype, void* stream);
+
 /* Message of the calling thread's last non-OK status ("" if none). */
 JEPA_API const char* jepa_last_error(void);
 JEPA_API int jepa_abi_version(void);

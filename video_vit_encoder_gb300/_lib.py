@@ -65,6 +65,7 @@ SIGNATURES = {
     "jepa_linear": (ST, [VP, VP, VP, VP, I, I, I, I, I, VP]),
     "jepa_ops_sync": (ST, [VP]),
     "jepa_selftest_wait_timeout": (ST, [I, VP]),
+    "jepa_patch_embed_static": (ST, [VP, VP, VP, VP, VP, I, I, I, I, I, I, VP]),
     "jepa_last_error": (C.c_char_p, []),
     "jepa_abi_version": (C.c_int, []),
 }

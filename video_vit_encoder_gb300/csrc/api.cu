@@ -507,6 +507,11 @@ jepa_status read_status(int* d_status, cudaStream_t s) {
 
 }  // namespace
 
+namespace jepa {
+// Lets other translation units set the message returned by jepa_last_error().
+void record_error(const char* msg) { g_last_error = msg; }
+}  // namespace jepa
+
 // ============================================================================= encoder
 struct jepa_encoder {
   jepa_encoder_params p{};
