@@ -1,42 +1,45 @@
 // Tensor-core attention for sm_103a, softmax(scale q k^T) v per (clip, head).
 //
-// One CTA owns 128 query rows of one (clip, head).  Keys and values stream
-// in tiles of 128 through a TMA ring.  Per tile j:
-//   S_j = Q K_j^T   tcgen05.mma into one of two TMEM score buffers (fp32);
-//   softmax warps (one thread per query row) read S_j, update the running
-//   max m and sum l in fp32, write P_j = exp2(S_j - m) as 16-bit into
-//   128B-swizzled shared memory;
-//   O += P_j V_j    tcgen05.mma into the TMEM output accumulator.
-// The running max is only moved (and O rescaled through TMEM) when it grows
-// by more than 2^8, so most tiles skip the rescale; m, l and O stay
-// consistent, and the final O / l is exact up to rounding.
-// V arrives transposed ([hd, keys], keys contiguous), so every MMA operand is
-// K-major.
+// One CTA owns two 128-row query tiles (Q0, Q1) of one (clip, head).  Keys
+// and values stream in tiles of 128 through a 3-deep TMA ring shared by both
+// query tiles.  For query tile t and key tile j:
+//   S_t = Q_t K_j^T     tcgen05.mma into TMEM (fp32, 128 lanes x 128 columns);
+//   softmax warpgroup t (one thread per query row) reads S_t from TMEM twice
+//   (row max, then the exponentials), updates the running max m and sum l in
+//   fp32, writes P_t = 2^((S_t - m) scale log2e) as 16-bit values into
+//   128B-swizzled shared memory and releases the TMEM buffer;
+//   O_t += P_t V_j      tcgen05.mma into the TMEM output accumulator.
+// The MMA warp alternates between the two tiles, so the tensor core works on
+// one tile while the other tile's softmax runs.  The running max is moved
+// (and O_t rescaled through TMEM) only when a row's max grows by more than
+// 2^8 in the exponent; m, l and O stay consistent, so O / l is exact up to
+// rounding.  V arrives transposed ([hd, keys], keys contiguous): every MMA
+// operand is K-major.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer and
-// tensor-memory owner, warps 2-5 softmax and output (warp w owns TMEM lanes
-// and query rows 32*(w%4) .. +31).
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and
+// tensor-memory owner, warps 2-5 softmax of Q0, warps 6-9 softmax of Q1
+// (warp w owns TMEM lanes / query rows 32*(w%4) .. +31 of its tile).
 #include "internal.h"
 
 namespace jepa {
 
 namespace {
 
-constexpr int kBQ = 128;     // query rows per CTA
+constexpr int kBQ = 128;     // query rows per tile (two tiles per CTA)
 constexpr int kBKV = 128;    // keys per tile
 constexpr int kStages = 3;   // K/V ring depth
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256, 256+HD)
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O0 [256,256+HD) O1 [384,384+HD)
 
 template <int HD>
 struct AttnSmem {
-  static constexpr uint32_t kQBytes = kBQ * HD * 2;
+  static constexpr uint32_t kQBytes = kBQ * HD * 2;    // one query tile
   static constexpr uint32_t kKBytes = kBKV * HD * 2;
-  static constexpr uint32_t kVBytes = HD * kBKV * 2;    // two 64-key blocks of HD rows x 128 B
+  static constexpr uint32_t kVBytes = HD * kBKV * 2;   // two 64-key blocks of HD rows x 128 B
   static constexpr uint32_t kVBlock = HD * 128;
-  static constexpr uint32_t kPBytes = kBQ * kBKV * 2;   // two 64-key blocks of 128 rows x 128 B
+  static constexpr uint32_t kPBytes = kBQ * kBKV * 2;  // two 64-key blocks of 128 rows x 128 B
   static constexpr uint32_t kPBlock = kBQ * 128;
-  static constexpr uint32_t kOffK = kQBytes;
+  static constexpr uint32_t kOffK = 2 * kQBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kKBytes;
   static constexpr uint32_t kOffP = kOffV + kStages * kVBytes;
   static constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
@@ -45,6 +48,11 @@ struct AttnSmem {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <typename T, int HD>
@@ -64,16 +72,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;   // [2]
-  uint64_t* p_full = s_full + 2;           // [2]
-  uint64_t* pv_done = p_full + 2;          // [2]
+  uint64_t* s_full = kv_empty + kStages;  // [2] per query tile
+  uint64_t* s_free = s_full + 2;          // [2]
+  uint64_t* p_full = s_free + 2;          // [2]
+  uint64_t* pv_done = p_full + 2;         // [2]
   uint64_t* mma_done = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
-  const int q0 = blockIdx.x * kBQ;
+  const int q0 = blockIdx.x * (2 * kBQ);
   const int n_kv = (n_tok + kBKV - 1) / kBKV;
 
   if (threadIdx.x == 0) {
@@ -84,6 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
       mbar_init(&p_full[i], 128);
       mbar_init(&pv_done[i], 1);
     }
@@ -102,13 +112,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_O = tmem + 256;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, S::kQBytes);
+      mbar_arrive_expect_tx(q_full, 2 * S::kQBytes);
       tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
+      tma_load_3d(sQ + S::kQBytes, &tmQ, q_full, 0, q0 + kBQ, bh);
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -144,41 +154,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_f16<T, kBQ, kBKV>();
       constexpr uint32_t idesc_o = idesc_f16<T, kBQ, HD>();
       bool ok = mbar_wait(q_full, 0);
-      const uint32_t aq = smem_u32(sQ);
+      // Per key tile j: S0_j, PV0_{j-1}, S1_j, PV1_{j-1}; the last round only PVs.
       for (int j = 0; ok && j <= n_kv && !*abort_flag; ++j) {
-        if (j < n_kv) {
-          const int stage = j % kStages;
-          if (!mbar_wait(&kv_full[stage], (j / kStages) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t ak = smem_u32(sK + stage * S::kKBytes);
-          const uint32_t d = tmem + (j & 1) * kBKV;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j < n_kv) {
+            const int stage = j % kStages;
+            if (t == 0 && !mbar_wait(&kv_full[stage], (j / kStages) & 1)) {
+              ok = false;
+              break;
+            }
+            // S_t is free once its softmax has copied S_t of key tile j-1 to registers.
+            if (j >= 1 && !mbar_wait(&s_free[t], (j - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t aq = smem_u32(sQ + t * S::kQBytes);
+            const uint32_t ak = smem_u32(sK + stage * S::kKBytes);
 #pragma unroll
-          for (int k = 0; k < HD / 16; ++k)
-            umma_f16_ss(d, smem_desc_kmajor<kQKRow>(aq + k * 32), smem_desc_kmajor<kQKRow>(ak + k * 32), idesc_s,
-                        k != 0);
-          umma_commit(&s_full[j & 1]);
-        }
-        if (j >= 1) {
-          const int jp = j - 1;
-          if (!mbar_wait(&p_full[jp & 1], (jp >> 1) & 1)) {
-            ok = false;
-            break;
+            for (int k = 0; k < HD / 16; ++k)
+              umma_f16_ss(tmem + t * kBKV, smem_desc_kmajor<kQKRow>(aq + k * 32),
+                          smem_desc_kmajor<kQKRow>(ak + k * 32), idesc_s, k != 0);
+            umma_commit(&s_full[t]);
           }
-          tc_fence_after();
-          const int stage = jp % kStages;
-          const uint32_t ap = smem_u32(sP + (jp & 1) * S::kPBytes);
-          const uint32_t av = smem_u32(sV + stage * S::kVBytes);
+          if (j >= 1) {
+            const int jp = j - 1;
+            if (!mbar_wait(&p_full[t], jp & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int stage = jp % kStages;
+            const uint32_t ap = smem_u32(sP + t * S::kPBytes);
+            const uint32_t av = smem_u32(sV + stage * S::kVBytes);
 #pragma unroll
-          for (int k = 0; k < kBKV / 16; ++k) {
-            const uint32_t off = (k & 3) * 32;
-            umma_f16_ss(tmem_O, smem_desc_kmajor<128>(ap + (k >> 2) * S::kPBlock + off),
-                        smem_desc_kmajor<128>(av + (k >> 2) * S::kVBlock + off), idesc_o, (jp | k) != 0);
+            for (int k = 0; k < kBKV / 16; ++k) {
+              const uint32_t off = (k & 3) * 32;
+              umma_f16_ss(tmem + 256 + t * 128, smem_desc_kmajor<128>(ap + (k >> 2) * S::kPBlock + off),
+                          smem_desc_kmajor<128>(av + (k >> 2) * S::kVBlock + off), idesc_o, (jp | k) != 0);
+            }
+            umma_commit(&pv_done[t]);
+            if (t == 1) umma_commit(&kv_empty[stage]);
           }
-          umma_commit(&kv_empty[stage]);
-          umma_commit(&pv_done[jp & 1]);
         }
       }
       if (!ok) {
@@ -189,107 +206,111 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(mma_done, 0);
     }
   } else {
-    // ------------------------------------------------------------ softmax + output
+    // ------------------------------------------------------------ softmax + output (tile t)
+    const int t = (warp - 2) >> 2;
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;          // row in tile = TMEM lane
+    const int r = quarter * 32 + lane;  // row in tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    float m = -INFINITY, l = 0.f;
+    const uint32_t tS = tmem + lane_off + t * kBKV;
+    const uint32_t tO = tmem + lane_off + 256 + t * 128;
+    uint8_t* pb = sP + t * S::kPBytes + r * 128;
+    float m = -INFINITY;  // running max of the raw scores
+    float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const bool w_ok = mbar_wait(&s_full[j & 1], (j >> 1) & 1);
+      const bool w_ok = mbar_wait(&s_full[t], j & 1);
       // tcgen05.ld/st are warp-collective: every decision that guards them is warp-uniform.
       if (__any_sync(0xffffffffu, !w_ok || *abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[kBKV];
+      const int kvalid = n_tok - j * kBKV;   // keys of this tile inside the sequence
+      // pass 1: row max of S_t, read from TMEM 64 columns at a time
+      float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kBKV / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_off + (j & 1) * kBKV + c * 32, u);
+      for (int c = 0; c < kBKV / 32; c += 2) {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tS + c * 32, u0);
+        tmem_ld32(tS + (c + 1) * 32, u1);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]) * scale_log2;
+        for (int i = 0; i < 32; ++i) {
+          mx = fmaxf(mx, (c * 32 + i < kvalid) ? __uint_as_float(u0[i]) : -INFINITY);
+          mx = fmaxf(mx, ((c + 1) * 32 + i < kvalid) ? __uint_as_float(u1[i]) : -INFINITY);
+        }
       }
-      const int kvalid = n_tok - j * kBKV;
-      if (kvalid < kBKV) {
-#pragma unroll
-        for (int i = 0; i < kBKV; ++i)
-          if (i >= kvalid) s[i] = -INFINITY;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int i = 1; i < kBKV; ++i) mx = fmaxf(mx, s[i]);
       if (j == 0) m = mx;
-      // Move the running max of the whole warp's rows when any of them grew by
-      // more than 2^8: O and l are rescaled by 2^(m_old - m_new) (1 for rows
-      // whose max did not grow).
-      if (__any_sync(0xffffffffu, j > 0 && mx > m + 8.0f)) {
+      // Move the running max of the warp's rows when any grew by more than 2^8
+      // (in the exponent): O and l are rescaled by 2^((m_old - m_new) scale log2e).
+      if (__any_sync(0xffffffffu, j > 0 && (mx - m) * scale_log2 > 8.0f)) {
         const float m_new = fmaxf(m, mx);
-        const float corr = exp2f(m - m_new);
-        const int jp = j - 1;
-        if (!mbar_wait(&pv_done[jp & 1], (jp >> 1) & 1)) ok = false;
+        const float corr = ex2((m - m_new) * scale_log2);
+        if (!mbar_wait(&pv_done[t], (j - 1) & 1)) ok = false;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t u[32];
-          tmem_ld32(tmem_O + lane_off + c * 32, u);
+          tmem_ld32(tO + c * 32, u);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * corr);
-          tmem_st32(tmem_O + lane_off + c * 32, u);
+          tmem_st32(tO + c * 32, u);
         }
         tmem_wait_st();
         l *= corr;
         m = m_new;
       }
-      // P_j may overwrite its buffer only after PV_{j-2} has read it.
-      if (j >= 2) {
-        const int jq = j - 2;
-        if (!mbar_wait(&pv_done[jq & 1], (jq >> 1) & 1)) ok = false;
-      }
-      uint8_t* pb = sP + (j & 1) * S::kPBytes + r * 128;
+      const float neg_m = -m * scale_log2;
+      // P_t's buffer is free once PV_t of the previous key tile has read it.
+      if (j >= 1 && !mbar_wait(&pv_done[t], (j - 1) & 1)) ok = false;
+      // pass 2: P = 2^(S scale log2e - m scale log2e), 16-bit, into swizzled smem
       float rs = 0.f;
 #pragma unroll
-      for (int c = 0; c < kBKV / 8; ++c) {
-        float p[8];
+      for (int c = 0; c < kBKV / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tS + c * 32, u);
+        tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          p[i] = exp2f(s[c * 8 + i] - m);
-          rs += p[i];
+        for (int g = 0; g < 4; ++g) {
+          float p[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int col = c * 32 + g * 8 + i;
+            p[i] = col < kvalid ? ex2(fmaf(__uint_as_float(u[g * 8 + i]), scale_log2, neg_m)) : 0.f;
+            rs += p[i];
+          }
+          uint4 w;
+          w.x = pack2<T>(p[0], p[1]);
+          w.y = pack2<T>(p[2], p[3]);
+          w.z = pack2<T>(p[4], p[5]);
+          w.w = pack2<T>(p[6], p[7]);
+          const int ch = (c & 1) * 4 + g;   // 16-byte chunk within the 128-byte row of block c/2
+          *reinterpret_cast<uint4*>(pb + (c >> 1) * S::kPBlock + ((ch ^ (r & 7)) << 4)) = w;
         }
-        uint4 w;
-        w.x = pack2<T>(p[0], p[1]);
-        w.y = pack2<T>(p[2], p[3]);
-        w.z = pack2<T>(p[4], p[5]);
-        w.w = pack2<T>(p[6], p[7]);
-        const int blk = c >> 3, ch = c & 7;
-        *reinterpret_cast<uint4*>(pb + blk * S::kPBlock + ((ch ^ (r & 7)) << 4)) = w;
       }
+      tc_fence_before();
+      mbar_arrive(&s_free[t]);  // S_t has been read: the MMA warp may overwrite it
       l += rs;
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[j & 1]);
+      mbar_arrive(&p_full[t]);
       if (__any_sync(0xffffffffu, !ok)) break;
     }
-    if (ok) {
-      const int jl = n_kv - 1;
-      ok = mbar_wait(&pv_done[jl & 1], (jl >> 1) & 1);
-    }
+    if (ok) ok = mbar_wait(&pv_done[t], (n_kv - 1) & 1);
     if (__any_sync(0xffffffffu, !ok)) {
       if (lane == 0) atomicOr(status, DEV_TIMEOUT);
       *abort_flag = 1;
     } else {
       tc_fence_after();
-      const int row = q0 + r;
+      const int row = q0 + t * kBQ + r;
       const float inv = 1.0f / l;
       const int b = bh / n_head, head = bh - (bh / n_head) * n_head;
       T* op = out + ((size_t)b * n_tok + row) * (size_t)(n_head * HD) + head * HD;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t u[32];
-        tmem_ld32(tmem_O + lane_off + c * 32, u);
+        tmem_ld32(tO + c * 32, u);
         tmem_wait_ld();
         if (row < n_tok) {
 #pragma unroll
@@ -333,7 +354,7 @@ cudaError_t launch_t(const void* q, const void* k, const void* vt, void* out, in
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid((n_tok + kBQ - 1) / kBQ, (unsigned)BH);
+  dim3 grid((n_tok + 2 * kBQ - 1) / (2 * kBQ), (unsigned)BH);
   kern<<<grid, kThreads, S::kBytes, s>>>(tq, tk, tv, (T*)out, n_head, n_tok, scale * 1.4426950408889634f, status);
   return cudaGetLastError();
 }

@@ -31,7 +31,97 @@ struct GemmSmem {
   static constexpr size_t kBytes = 1024 /*alignment slack*/ + (size_t)STAGES * kStageBytes + 256;
 };
 
-template <typename T, int BN, int STAGES, int EPI>
+// QKV epilogue of one thread's row of a 128 x BN accumulator tile.  BN
+// divides D, so the whole tile lies in the q, the k or the v section.  The
+// token's RoPE factors (3 axes x d/2 angles, cos and sin) are loaded once per
+// tile and shared by the tile's BN/HD heads; with HD and the layout fixed at
+// compile time every axis / angle index below is a constant.
+//   out[2k]   = x[2k]   cos(a_f0) - x[2k+1] sin(a_f0)
+//   out[2k+1] = x[2k+1] cos(a_f1) + x[2k]   sin(a_f1)
+// with f0 = f1 = k' (interleaved) or f0 = 2k' mod d/2, f1 = (2k'+1) mod d/2
+// (tiled), k' the pair index within its axis segment.
+template <typename T, int BN, int HD, int LAYOUT>
+__device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t taddr, int row, bool row_ok,
+                                                  int col_base) {
+  static_assert(HD == 32 || HD == 64, "head dim");
+  static_assert(BN % HD == 0, "tile must hold whole heads");
+  constexpr int RD = 2 * ((HD / 3) / 2);
+  constexpr int HALF = RD / 2;
+  const int D = ep.dmodel;
+  const int which = col_base / D;
+  const int head0 = (col_base - which * D) / HD;
+  const int clip = row / ep.n_tok;
+  const int tok = row - clip * ep.n_tok;
+  float cz[3][HALF], sz[3][HALF];
+  if (which < 2) {
+    int p[3] = {0, 0, 0};
+    if (row_ok) {
+      const int gid = ep.pos_ids != nullptr ? __ldg(ep.pos_ids + row) : tok;
+      const int plane = ep.rope.gh * ep.rope.gw;
+      p[0] = gid / plane;
+      const int rem = gid - p[0] * plane;
+      p[1] = rem / ep.rope.gw;
+      p[2] = rem - p[1] * ep.rope.gw;
+    }
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      const float* ct = ep.rope.cos_tab + (a * ep.rope.max_pos + p[a]) * HALF;
+      const float* st = ep.rope.sin_tab + (a * ep.rope.max_pos + p[a]) * HALF;
+#pragma unroll
+      for (int k = 0; k < HALF; ++k) {
+        cz[a][k] = __ldg(ct + k);
+        sz[a][k] = __ldg(st + k);
+      }
+    }
+  }
+  const size_t bh0 = (size_t)clip * ep.n_head + head0;
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c * 32, r);
+    tmem_wait_ld();
+    if (!row_ok) continue;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    if (ep.bias != nullptr) {
+      const float* b = ep.bias + col_base + c * 32;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 bb = __ldg(reinterpret_cast<const float4*>(b + i));
+        v[i] += bb.x;
+        v[i + 1] += bb.y;
+        v[i + 2] += bb.z;
+        v[i + 3] += bb.w;
+      }
+    }
+    const int d0 = (c * 32) % HD;
+    const size_t bh = bh0 + (c * 32) / HD;
+    if (which < 2) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const int dim = d0 + j;
+        if (dim < 3 * RD) {
+          const int a = dim / RD;
+          const int jj = dim - a * RD;
+          const int f0 = LAYOUT == 0 ? jj % HALF : jj / 2;
+          const int f1 = LAYOUT == 0 ? (jj + 1) % HALF : jj / 2;
+          const float x0 = v[j], x1 = v[j + 1];
+          v[j] = x0 * cz[a][f0] - x1 * sz[a][f0];
+          v[j + 1] = x1 * cz[a][f1] + x0 * sz[a][f1];
+        }
+      }
+      T* dst = reinterpret_cast<T*>(which == 0 ? ep.q : ep.k) + (bh * ep.n_tok + tok) * HD + d0;
+      store_row_chunk<T, 32>(dst, v);
+    } else {
+      T* dst = reinterpret_cast<T*>(ep.vt) + (bh * HD + d0) * (size_t)ep.ldv + tok;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[(size_t)i * ep.ldv] = DT<T>::from(v[i]);
+    }
+  }
+}
+
+template <typename T, int BN, int STAGES, int EPI, int QHD = 0, int QLAYOUT = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
                    int K, EpiParams ep, int* status) {
@@ -177,6 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int tm = tile / num_n, tn = tile - tm * num_n;
       const int row = tm * kBM + row_in_tile;
+      if constexpr (EPI == EPI_QKV) {
+        qkv_tile_epilogue<T, BN, QHD, QLAYOUT>(ep, tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN, row,
+                                               row < M, tn * BN);
+      } else {
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -189,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
           epilogue_apply<T, EPI, 32>(ep, row, col0, v);
         }
+      }
       }
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
@@ -203,11 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename T, int BN, int STAGES, int EPI>
+template <typename T, int BN, int STAGES, int EPI, int QHD = 0, int QLAYOUT = 0>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
                        int* status, cudaStream_t stream, int num_sms) {
   using S = GemmSmem<BN, STAGES>;
-  auto kern = gemm_tc_kernel<T, BN, STAGES, EPI>;
+  auto kern = gemm_tc_kernel<T, BN, STAGES, EPI, QHD, QLAYOUT>;
   static bool configured = false;  // per instantiation
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
@@ -228,7 +323,12 @@ cudaError_t dispatch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, 
     case EPI_F32: return launch_one<T, BN, STAGES, EPI_F32>(ta, tb, M, N, K, ep, status, s, sms);
     case EPI_RESID: return launch_one<T, BN, STAGES, EPI_RESID>(ta, tb, M, N, K, ep, status, s, sms);
     case EPI_GELU: return launch_one<T, BN, STAGES, EPI_GELU>(ta, tb, M, N, K, ep, status, s, sms);
-    case EPI_QKV: return launch_one<T, BN, STAGES, EPI_QKV>(ta, tb, M, N, K, ep, status, s, sms);
+    case EPI_QKV:
+      if (ep.head_dim == 64)
+        return ep.rope.layout == 0 ? launch_one<T, BN, STAGES, EPI_QKV, 64, 0>(ta, tb, M, N, K, ep, status, s, sms)
+                                   : launch_one<T, BN, STAGES, EPI_QKV, 64, 1>(ta, tb, M, N, K, ep, status, s, sms);
+      return ep.rope.layout == 0 ? launch_one<T, BN, STAGES, EPI_QKV, 32, 0>(ta, tb, M, N, K, ep, status, s, sms)
+                                 : launch_one<T, BN, STAGES, EPI_QKV, 32, 1>(ta, tb, M, N, K, ep, status, s, sms);
   }
   return cudaErrorInvalidValue;
 }
