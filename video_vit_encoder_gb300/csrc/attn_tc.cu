@@ -54,6 +54,92 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Two fp32 values in one 64-bit register pair, for the packed f32x2 pipes.
+__device__ __forceinline__ uint64_t pk2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Row max of one S tile (128 columns in TMEM from taddr); columns >= kvalid
+// are ignored when MASK.
+template <bool MASK>
+__device__ __forceinline__ float tile_row_max(uint32_t taddr, int kvalid) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < kBKV / 32; c += 2) {
+    uint32_t u0[32], u1[32];
+    tmem_ld32(taddr + c * 32, u0);
+    tmem_ld32(taddr + (c + 1) * 32, u1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float a = __uint_as_float(u0[i]), b = __uint_as_float(u1[i]);
+      if (MASK) {
+        a = (c * 32 + i < kvalid) ? a : -INFINITY;
+        b = ((c + 1) * 32 + i < kvalid) ? b : -INFINITY;
+      }
+      mx = max3(mx, a, b);
+    }
+  }
+  return mx;
+}
+
+// P = 2^(S scale_log2 + neg_m) for one S tile, as 16-bit values into the
+// thread's 128B-swizzled smem row pb; returns the row sum of P (fp32).
+template <typename T, bool MASK, uint32_t kPBlock>
+__device__ __forceinline__ float tile_exp_store(uint32_t taddr, int kvalid, float scale_log2, float neg_m,
+                                                uint8_t* pb, int r) {
+  const uint64_t sc2 = pk2(__float_as_uint(scale_log2), __float_as_uint(scale_log2));
+  const uint64_t nm2 = pk2(__float_as_uint(neg_m), __float_as_uint(neg_m));
+  uint64_t rs2 = 0;  // (0.f, 0.f)
+#pragma unroll
+  for (int c = 0; c < kBKV / 32; ++c) {
+    uint32_t u[32];
+    tmem_ld32(taddr + c * 32, u);
+    tmem_wait_ld();
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        float x0, x1;
+        upk2(fma2(pk2(u[g * 8 + i], u[g * 8 + i + 1]), sc2, nm2), x0, x1);
+        float p0 = ex2(x0), p1 = ex2(x1);
+        if (MASK) {
+          const int col = c * 32 + g * 8 + i;
+          p0 = col < kvalid ? p0 : 0.f;
+          p1 = col + 1 < kvalid ? p1 : 0.f;
+        }
+        rs2 = add2(rs2, pk2(__float_as_uint(p0), __float_as_uint(p1)));
+        w[i / 2] = pack2<T>(p0, p1);
+      }
+      const int ch = (c & 1) * 4 + g;  // 16-byte chunk within the 128-byte row of block c/2
+      *reinterpret_cast<uint4*>(pb + (c >> 1) * kPBlock + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  float a, b;
+  upk2(rs2, a, b);
+  return a + b;
+}
 
 template <typename T, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -227,19 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int kvalid = n_tok - j * kBKV;   // keys of this tile inside the sequence
       // pass 1: row max of S_t, read from TMEM 64 columns at a time
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kBKV / 32; c += 2) {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(tS + c * 32, u0);
-        tmem_ld32(tS + (c + 1) * 32, u1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          mx = fmaxf(mx, (c * 32 + i < kvalid) ? __uint_as_float(u0[i]) : -INFINITY);
-          mx = fmaxf(mx, ((c + 1) * 32 + i < kvalid) ? __uint_as_float(u1[i]) : -INFINITY);
-        }
-      }
+      const float mx = kvalid >= kBKV ? tile_row_max<false>(tS, kvalid) : tile_row_max<true>(tS, kvalid);
       if (j == 0) m = mx;
       // Move the running max of the warp's rows when any grew by more than 2^8
       // (in the exponent): O and l are rescaled by 2^((m_old - m_new) scale log2e).
@@ -264,31 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float neg_m = -m * scale_log2;
       // P_t's buffer is free once PV_t of the previous key tile has read it.
       if (j >= 1 && !mbar_wait(&pv_done[t], (j - 1) & 1)) ok = false;
-      // pass 2: P = 2^(S scale log2e - m scale log2e), 16-bit, into swizzled smem
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < kBKV / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tS + c * 32, u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float p[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int col = c * 32 + g * 8 + i;
-            p[i] = col < kvalid ? ex2(fmaf(__uint_as_float(u[g * 8 + i]), scale_log2, neg_m)) : 0.f;
-            rs += p[i];
-          }
-          uint4 w;
-          w.x = pack2<T>(p[0], p[1]);
-          w.y = pack2<T>(p[2], p[3]);
-          w.z = pack2<T>(p[4], p[5]);
-          w.w = pack2<T>(p[6], p[7]);
-          const int ch = (c & 1) * 4 + g;   // 16-byte chunk within the 128-byte row of block c/2
-          *reinterpret_cast<uint4*>(pb + (c >> 1) * S::kPBlock + ((ch ^ (r & 7)) << 4)) = w;
-        }
-      }
+      // pass 2: P = 2^((S - m) scale log2e), 16-bit, into swizzled smem
+      const float rs = kvalid >= kBKV
+                           ? tile_exp_store<T, false, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r)
+                           : tile_exp_store<T, true, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r);
       tc_fence_before();
       mbar_arrive(&s_free[t]);  // S_t has been read: the MMA warp may overwrite it
       l += rs;

@@ -121,7 +121,7 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
   }
 }
 
-template <typename T, int BN, int STAGES, int EPI, int QHD = 0, int QLAYOUT = 0>
+template <typename T, int BN, int STAGES, int EPI, int QHD = 0, int QLAYOUT = 0, int CM = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
                    int K, EpiParams ep, int* status) {
@@ -141,13 +141,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_n = (N + BN - 1) / BN;
-  const int num_tiles = ((M + kBM - 1) / kBM) * num_n;
+  // Work units: CM vertically adjacent 128 x BN tiles (same W rows).  With a
+  // 2-CTA cluster each CTA computes one tile of the unit and TMA-multicasts
+  // its half of the shared W tile to both CTAs.
+  const int num_units = ((M + kBM * CM - 1) / (kBM * CM)) * num_n;
   const int num_kb = K / kBK;
+  const int rank = CM == 2 ? (int)cluster_ctarank() : 0;
+  const int first_unit = CM == 2 ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int unit_stride = CM == 2 ? (int)cluster_count_x() : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CM);   // released by the MMA of every CTA that reads the stage
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -164,7 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CM == 2) {
+    cluster_sync();   // the peer's barriers are initialised before any multicast signal
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -174,8 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       long issued = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
-        const int tm = tile / num_n, tn = tile - tm * num_n;
+      for (int u = first_unit; u < num_units && !*abort_flag; u += unit_stride) {
+        const int mp = u / num_n, tn = u - mp * num_n;
+        const int tm = mp * CM + rank;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             atomicOr(status, DEV_TIMEOUT);
@@ -184,7 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
           tma_load_2d(sA + stage * S::kABytes, &tmA, &full[stage], kb * kBK, tm * kBM);
-          tma_load_2d(sB + stage * S::kBBytes, &tmB, &full[stage], kb * kBK, tn * BN);
+          if constexpr (CM == 2) {
+            tma_load_2d_multicast(sB + stage * S::kBBytes + rank * (S::kBBytes / 2), &tmB, &full[stage], kb * kBK,
+                                  tn * BN + rank * (BN / 2), (uint16_t)0x3);
+          } else {
+            tma_load_2d(sB + stage * S::kBBytes, &tmB, &full[stage], kb * kBK, tn * BN);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -210,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++acc) {
+      for (int u = first_unit; u < num_units && !*abort_flag; u += unit_stride, ++acc) {
         const int buf = acc & 1;
         const uint32_t acc_phase = (acc >> 1) & 1;
         if (!mbar_wait(&tempty[buf], acc_phase ^ 1)) {
@@ -236,7 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_f16_ss(d_tmem, smem_desc_kmajor<128>(a0 + k * 32), smem_desc_kmajor<128>(b0 + k * 32), idesc,
                         (kb | k) != 0);
           }
-          umma_commit(&empty[stage]);
+          if constexpr (CM == 2) {
+            umma_commit_multicast(&empty[stage], (uint16_t)0x3);
+          } else {
+            umma_commit(&empty[stage]);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -254,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
     int acc = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++acc) {
+    for (int u = first_unit; u < num_units; u += unit_stride, ++acc) {
       const int buf = acc & 1;
       const uint32_t acc_phase = (acc >> 1) & 1;
       const bool ok = mbar_wait(&tfull[buf], acc_phase);
@@ -265,8 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int tm = tile / num_n, tn = tile - tm * num_n;
-      const int row = tm * kBM + row_in_tile;
+      const int mp = u / num_n, tn = u - mp * num_n;
+      const int row = (mp * CM + rank) * kBM + row_in_tile;
       if constexpr (EPI == EPI_QKV) {
         qkv_tile_epilogue<T, BN, QHD, QLAYOUT>(ep, tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN, row,
                                                row < M, tn * BN);
@@ -296,20 +316,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, S::kTmemCols);
   }
+  if constexpr (CM == 2) cluster_sync();   // no peer signal may target this CTA after it exits
 }
 
 template <typename T, int BN, int STAGES, int EPI, int QHD = 0, int QLAYOUT = 0>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
-                       int* status, cudaStream_t stream, int num_sms) {
+                       int* status, cudaStream_t stream, int num_sms, int cm) {
   using S = GemmSmem<BN, STAGES>;
-  auto kern = gemm_tc_kernel<T, BN, STAGES, EPI, QHD, QLAYOUT>;
+  const int num_m = (M + kBM - 1) / kBM, num_n = (N + BN - 1) / BN;
+  if (cm == 2) {
+    auto kern = gemm_tc_kernel<T, BN, STAGES, EPI, QHD, QLAYOUT, 2>;
+    static bool configured = false;  // per instantiation
+    if (!configured) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    const int units = ((num_m + 1) / 2) * num_n;
+    const int clusters = units < num_sms / 2 ? units : num_sms / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = S::kBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, M, N, K, ep, status);
+  }
+  auto kern = gemm_tc_kernel<T, BN, STAGES, EPI, QHD, QLAYOUT, 1>;
   static bool configured = false;  // per instantiation
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
+  const int tiles = num_m * num_n;
   const int grid = tiles < num_sms ? tiles : num_sms;
   kern<<<grid, kThreads, S::kBytes, stream>>>(ta, tb, M, N, K, ep, status);
   return cudaGetLastError();
@@ -317,18 +363,19 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, int M, int 
 
 template <typename T, int BN, int STAGES>
 cudaError_t dispatch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
-                         const EpiParams& ep, int* status, cudaStream_t s, int sms) {
+                         const EpiParams& ep, int* status, cudaStream_t s, int sms, int cm) {
   switch (epi) {
-    case EPI_STORE: return launch_one<T, BN, STAGES, EPI_STORE>(ta, tb, M, N, K, ep, status, s, sms);
-    case EPI_F32: return launch_one<T, BN, STAGES, EPI_F32>(ta, tb, M, N, K, ep, status, s, sms);
-    case EPI_RESID: return launch_one<T, BN, STAGES, EPI_RESID>(ta, tb, M, N, K, ep, status, s, sms);
-    case EPI_GELU: return launch_one<T, BN, STAGES, EPI_GELU>(ta, tb, M, N, K, ep, status, s, sms);
+    case EPI_STORE: return launch_one<T, BN, STAGES, EPI_STORE>(ta, tb, M, N, K, ep, status, s, sms, cm);
+    case EPI_F32: return launch_one<T, BN, STAGES, EPI_F32>(ta, tb, M, N, K, ep, status, s, sms, cm);
+    case EPI_RESID: return launch_one<T, BN, STAGES, EPI_RESID>(ta, tb, M, N, K, ep, status, s, sms, cm);
+    case EPI_GELU: return launch_one<T, BN, STAGES, EPI_GELU>(ta, tb, M, N, K, ep, status, s, sms, cm);
     case EPI_QKV:
       if (ep.head_dim == 64)
-        return ep.rope.layout == 0 ? launch_one<T, BN, STAGES, EPI_QKV, 64, 0>(ta, tb, M, N, K, ep, status, s, sms)
-                                   : launch_one<T, BN, STAGES, EPI_QKV, 64, 1>(ta, tb, M, N, K, ep, status, s, sms);
-      return ep.rope.layout == 0 ? launch_one<T, BN, STAGES, EPI_QKV, 32, 0>(ta, tb, M, N, K, ep, status, s, sms)
-                                 : launch_one<T, BN, STAGES, EPI_QKV, 32, 1>(ta, tb, M, N, K, ep, status, s, sms);
+        return ep.rope.layout == 0
+                   ? launch_one<T, BN, STAGES, EPI_QKV, 64, 0>(ta, tb, M, N, K, ep, status, s, sms, cm)
+                   : launch_one<T, BN, STAGES, EPI_QKV, 64, 1>(ta, tb, M, N, K, ep, status, s, sms, cm);
+      return ep.rope.layout == 0 ? launch_one<T, BN, STAGES, EPI_QKV, 32, 0>(ta, tb, M, N, K, ep, status, s, sms, cm)
+                                 : launch_one<T, BN, STAGES, EPI_QKV, 32, 1>(ta, tb, M, N, K, ep, status, s, sms, cm);
   }
   return cudaErrorInvalidValue;
 }
@@ -337,13 +384,15 @@ template <typename T>
 cudaError_t gemm_tc_typed(int epi, const void* A, const void* W, int M, int N, int K, const EpiParams& ep,
                           int* status, cudaStream_t s, int sms) {
   const int BN = (N % 256 == 0) ? 256 : 128;
+  // Pairs of CTAs share each W tile when there are at least two row tiles.
+  const int cm = M > kBM ? 2 : 1;
   CUtensorMap ta, tb;
   cudaError_t e = make_tmap_2d(&ta, A, sizeof(T), K, M, (size_t)K * sizeof(T), kBK, kBM);
   if (e != cudaSuccess) return e;
-  e = make_tmap_2d(&tb, W, sizeof(T), K, N, (size_t)K * sizeof(T), kBK, BN);
+  e = make_tmap_2d(&tb, W, sizeof(T), K, N, (size_t)K * sizeof(T), kBK, BN / cm);
   if (e != cudaSuccess) return e;
-  if (BN == 256) return dispatch_epi<T, 256, 4>(epi, ta, tb, M, N, K, ep, status, s, sms);
-  return dispatch_epi<T, 128, 6>(epi, ta, tb, M, N, K, ep, status, s, sms);
+  if (BN == 256) return dispatch_epi<T, 256, 4>(epi, ta, tb, M, N, K, ep, status, s, sms, cm);
+  return dispatch_epi<T, 128, 6>(epi, ta, tb, M, N, K, ep, status, s, sms, cm);
 }
 
 }  // namespace
