@@ -8,9 +8,11 @@
 // two accumulators in tensor memory so the epilogue of one tile overlaps the
 // main loop of the next.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer and
-// tensor-memory owner, warps 2-5 epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. 32*(w%4)+31).
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and
+// tensor-memory owner, warps 2-9 epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. 32*(w%4)+31 and column half (w-2)/4 of the tile).
+// With more than one row tile, CTAs run in clusters of two that share each
+// weight tile: each CTA loads half of it and TMA-multicasts it to both.
 #include "epilogue.cuh"
 #include "internal.h"
 
@@ -20,7 +22,8 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;  // 64 x 16-bit = one 128-byte swizzle row
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;   // warps 2-9
 
 template <int BN, int STAGES>
 struct GemmSmem {
@@ -42,14 +45,14 @@ struct GemmSmem {
 // (tiled), k' the pair index within its axis segment.
 template <typename T, int BN, int HD, int LAYOUT>
 __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t taddr, int row, bool row_ok,
-                                                  int col_base) {
+                                                  int col_base, int col_off) {
   static_assert(HD == 32 || HD == 64, "head dim");
-  static_assert(BN % HD == 0, "tile must hold whole heads");
+  static_assert((BN / 2) % HD == 0, "each half tile must hold whole heads");
   constexpr int RD = 2 * ((HD / 3) / 2);
   constexpr int HALF = RD / 2;
   const int D = ep.dmodel;
   const int which = col_base / D;
-  const int head0 = (col_base - which * D) / HD;
+  const int head0 = (col_base + col_off - which * D) / HD;   // first head of this thread's half tile
   const int clip = row / ep.n_tok;
   const int tok = row - clip * ep.n_tok;
   float cz[3][HALF], sz[3][HALF];
@@ -76,7 +79,7 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
   }
   const size_t bh0 = (size_t)clip * ep.n_head + head0;
 #pragma unroll
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = 0; c < BN / 64; ++c) {
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_wait_ld();
@@ -85,7 +88,7 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
     if (ep.bias != nullptr) {
-      const float* b = ep.bias + col_base + c * 32;
+      const float* b = ep.bias + col_base + col_off + c * 32;
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
         const float4 bb = __ldg(reinterpret_cast<const float4*>(b + i));
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
+      mbar_init(&tempty[i], kEpiThreads);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -271,7 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Eight warps: warp w drains TMEM lanes 32*(w%4) .. +31 (its rows) and the
+    // column half (w-2)/4 of the tile, so two warps per SM sub-partition share
+    // the epilogue work and hide each other's latency.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = quarter * 32 + lane;
     int acc = 0;
     for (int u = first_unit; u < num_units; u += unit_stride, ++acc) {
@@ -288,15 +295,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mp = u / num_n, tn = u - mp * num_n;
       const int row = (mp * CM + rank) * kBM + row_in_tile;
       if constexpr (EPI == EPI_QKV) {
-        qkv_tile_epilogue<T, BN, QHD, QLAYOUT>(ep, tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN, row,
-                                               row < M, tn * BN);
+        qkv_tile_epilogue<T, BN, QHD, QLAYOUT>(ep, tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN +
+                                                   half * (BN / 2),
+                                               row, row < M, tn * BN, half * (BN / 2));
       } else {
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < BN / 64; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + c * 32, r);
+        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2) + c * 32, r);
         tmem_wait_ld();
-        const int col0 = tn * BN + c * 32;
+        const int col0 = tn * BN + half * (BN / 2) + c * 32;
         if (row < M && col0 < N) {
           float v[32];
 #pragma unroll
