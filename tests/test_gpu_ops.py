@@ -125,8 +125,12 @@ def test_attention_tc(jg, dtype, hd, N, logit_std):
     B, H = 2, 3
     rng = np.random.default_rng(N + hd)
     q, k, v = _attn_inputs(rng, B, H, N, hd, dtype, logit_std)
-    if logit_std > 2:   # a planted large logit on a few rows
+    if logit_std > 2:
+        # planted large logits: query 3 meets its outlier key in the first key
+        # tile; query 130 only in the last one, which moves its running max
+        # late and exercises the rescale of the partial output
         k[:, 7] = synth.round_to_dtype(q[:, 3] * 3, dtype)
+        k[:, N - 5] = synth.round_to_dtype(q[:, 130] * 3, dtype)
     got = _run_attn(jg, q, k, v, B, H, N, hd, dtype)
     ref = oracle.attention_heads(q, k, v).reshape(B, H, N, hd).transpose(0, 2, 1, 3).reshape(B, N, H * hd)
     assert_close_16bit(got, ref, f"attention {dtype} hd{hd} N{N}")

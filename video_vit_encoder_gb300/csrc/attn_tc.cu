@@ -4,16 +4,17 @@
 // and values stream in tiles of 128 through a 3-deep TMA ring shared by both
 // query tiles.  For query tile t and key tile j:
 //   S_t = Q_t K_j^T     tcgen05.mma into TMEM (fp32, 128 lanes x 128 columns);
-//   softmax warpgroup t (one thread per query row) reads S_t from TMEM twice
-//   (row max, then the exponentials), updates the running max m and sum l in
-//   fp32, writes P_t = 2^((S_t - m) scale log2e) as 16-bit values into
-//   128B-swizzled shared memory and releases the TMEM buffer;
+//   softmax warpgroup t (one thread per query row) reads S_t from TMEM once
+//   (twice for the first key tile, whose row max starts the running max m),
+//   writes P_t = 2^((S_t - m) scale log2e) as 16-bit values into
+//   128B-swizzled shared memory, accumulates the row sum l in fp32 and
+//   releases the TMEM buffer;
 //   O_t += P_t V_j      tcgen05.mma into the TMEM output accumulator.
 // The MMA warp alternates between the two tiles, so the tensor core works on
 // one tile while the other tile's softmax runs.  The running max is moved
-// (and O_t rescaled through TMEM) only when a row's max grows by more than
-// 2^8 in the exponent; m, l and O stay consistent, so O / l is exact up to
-// rounding.  V arrives transposed ([hd, keys], keys contiguous): every MMA
+// (O_t and l rescaled, the tile's exponentials redone) only when a row's max
+// grows by more than 2^8 in the exponent; m, l and O stay consistent, so
+// O / l is exact up to rounding.  V arrives transposed ([hd, keys], keys contiguous): every MMA
 // operand is K-major.
 //
 // Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and
@@ -104,13 +105,17 @@ __device__ __forceinline__ float tile_row_max(uint32_t taddr, int kvalid) {
 }
 
 // P = 2^(S scale_log2 + neg_m) for one S tile, as 16-bit values into the
-// thread's 128B-swizzled smem row pb; returns the row sum of P (fp32).
+// thread's 128B-swizzled smem row pb (16-byte chunk ch of 64-column block b
+// goes to chunk ch ^ (row % 8)); returns the row sum of P (fp32) and, in
+// xmax, the largest exponent S scale_log2 + neg_m of the row (columns >=
+// kvalid excluded when MASK).
 template <typename T, bool MASK, uint32_t kPBlock>
 __device__ __forceinline__ float tile_exp_store(uint32_t taddr, int kvalid, float scale_log2, float neg_m,
-                                                uint8_t* pb, int r) {
+                                                uint8_t* pb, int r, float& xmax) {
   const uint64_t sc2 = pk2(__float_as_uint(scale_log2), __float_as_uint(scale_log2));
   const uint64_t nm2 = pk2(__float_as_uint(neg_m), __float_as_uint(neg_m));
   uint64_t rs2 = 0;  // (0.f, 0.f)
+  float xm = -INFINITY;
 #pragma unroll
   for (int c = 0; c < kBKV / 32; ++c) {
     uint32_t u[32];
@@ -123,12 +128,13 @@ __device__ __forceinline__ float tile_exp_store(uint32_t taddr, int kvalid, floa
       for (int i = 0; i < 8; i += 2) {
         float x0, x1;
         upk2(fma2(pk2(u[g * 8 + i], u[g * 8 + i + 1]), sc2, nm2), x0, x1);
-        float p0 = ex2(x0), p1 = ex2(x1);
         if (MASK) {
           const int col = c * 32 + g * 8 + i;
-          p0 = col < kvalid ? p0 : 0.f;
-          p1 = col + 1 < kvalid ? p1 : 0.f;
+          x0 = col < kvalid ? x0 : -INFINITY;
+          x1 = col + 1 < kvalid ? x1 : -INFINITY;
         }
+        xm = max3(xm, x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
         rs2 = add2(rs2, pk2(__float_as_uint(p0), __float_as_uint(p1)));
         w[i / 2] = pack2<T>(p0, p1);
       }
@@ -136,6 +142,7 @@ __device__ __forceinline__ float tile_exp_store(uint32_t taddr, int kvalid, floa
       *reinterpret_cast<uint4*>(pb + (c >> 1) * kPBlock + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
+  xmax = xm;
   float a, b;
   upk2(rs2, a, b);
   return a + b;
@@ -240,29 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_f16<T, kBQ, kBKV>();
       constexpr uint32_t idesc_o = idesc_f16<T, kBQ, HD>();
       bool ok = mbar_wait(q_full, 0);
-      // Per key tile j: S0_j, PV0_{j-1}, S1_j, PV1_{j-1}; the last round only PVs.
+      // Per key tile j: PV0_{j-1}, S0_j, PV1_{j-1}, S1_j (the last round only
+      // PVs).  Issuing PV_t before S_t means S_t's completion also covers PV_t.
       for (int j = 0; ok && j <= n_kv && !*abort_flag; ++j) {
         for (int t = 0; t < 2 && ok; ++t) {
-          if (j < n_kv) {
-            const int stage = j % kStages;
-            if (t == 0 && !mbar_wait(&kv_full[stage], (j / kStages) & 1)) {
-              ok = false;
-              break;
-            }
-            // S_t is free once its softmax has copied S_t of key tile j-1 to registers.
-            if (j >= 1 && !mbar_wait(&s_free[t], (j - 1) & 1)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t aq = smem_u32(sQ + t * S::kQBytes);
-            const uint32_t ak = smem_u32(sK + stage * S::kKBytes);
-#pragma unroll
-            for (int k = 0; k < HD / 16; ++k)
-              umma_f16_ss(tmem + t * kBKV, smem_desc_kmajor<kQKRow>(aq + k * 32),
-                          smem_desc_kmajor<kQKRow>(ak + k * 32), idesc_s, k != 0);
-            umma_commit(&s_full[t]);
-          }
           if (j >= 1) {
             const int jp = j - 1;
             if (!mbar_wait(&p_full[t], jp & 1)) {
@@ -281,6 +269,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             umma_commit(&pv_done[t]);
             if (t == 1) umma_commit(&kv_empty[stage]);
+          }
+          if (j < n_kv) {
+            const int stage = j % kStages;
+            if (t == 0 && !mbar_wait(&kv_full[stage], (j / kStages) & 1)) {
+              ok = false;
+              break;
+            }
+            // S_t is free once its softmax has read S_t of key tile j-1.
+            if (j >= 1 && !mbar_wait(&s_free[t], (j - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t aq = smem_u32(sQ + t * S::kQBytes);
+            const uint32_t ak = smem_u32(sK + stage * S::kKBytes);
+#pragma unroll
+            for (int k = 0; k < HD / 16; ++k)
+              umma_f16_ss(tmem + t * kBKV, smem_desc_kmajor<kQKRow>(aq + k * 32),
+                          smem_desc_kmajor<kQKRow>(ak + k * 32), idesc_s, k != 0);
+            umma_commit(&s_full[t]);
           }
         }
       }
@@ -312,15 +320,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int kvalid = n_tok - j * kBKV;   // keys of this tile inside the sequence
-      // pass 1: row max of S_t, read from TMEM 64 columns at a time
-      const float mx = kvalid >= kBKV ? tile_row_max<false>(tS, kvalid) : tile_row_max<true>(tS, kvalid);
-      if (j == 0) m = mx;
-      // Move the running max of the warp's rows when any grew by more than 2^8
-      // (in the exponent): O and l are rescaled by 2^((m_old - m_new) scale log2e).
-      if (__any_sync(0xffffffffu, j > 0 && (mx - m) * scale_log2 > 8.0f)) {
+      const bool full_tile = kvalid >= kBKV;
+      // The first key tile fixes the running max (one extra TMEM pass); later
+      // tiles are exponentiated against the running max in a single pass.
+      if (j == 0) m = full_tile ? tile_row_max<false>(tS, kvalid) : tile_row_max<true>(tS, kvalid);
+      float neg_m = -m * scale_log2;
+      // P_t's buffer is free (and O_t stable) once PV_t of the previous key
+      // tile is done; it was issued before S_t of this tile, so this wait
+      // normally returns at once.
+      if (j >= 1 && !mbar_wait(&pv_done[t], (j - 1) & 1)) ok = false;
+      float xmax;
+      float rs = full_tile ? tile_exp_store<T, false, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r, xmax)
+                           : tile_exp_store<T, true, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r, xmax);
+      if (__any_sync(0xffffffffu, xmax > 8.0f)) {
+        // Rare: a row's max grew by more than 2^8 in the exponent.  Move the
+        // running max of the warp's rows to the tile max, rescale O_t and l by
+        // 2^((m_old - m_new) scale log2e) (1 for rows whose max did not grow)
+        // and redo this tile's exponentials.
+        const float mx = full_tile ? tile_row_max<false>(tS, kvalid) : tile_row_max<true>(tS, kvalid);
         const float m_new = fmaxf(m, mx);
         const float corr = ex2((m - m_new) * scale_log2);
-        if (!mbar_wait(&pv_done[t], (j - 1) & 1)) ok = false;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
@@ -334,14 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         l *= corr;
         m = m_new;
+        neg_m = -m * scale_log2;
+        rs = full_tile ? tile_exp_store<T, false, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r, xmax)
+                       : tile_exp_store<T, true, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r, xmax);
       }
-      const float neg_m = -m * scale_log2;
-      // P_t's buffer is free once PV_t of the previous key tile has read it.
-      if (j >= 1 && !mbar_wait(&pv_done[t], (j - 1) & 1)) ok = false;
-      // pass 2: P = 2^((S - m) scale log2e), 16-bit, into swizzled smem
-      const float rs = kvalid >= kBKV
-                           ? tile_exp_store<T, false, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r)
-                           : tile_exp_store<T, true, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r);
       tc_fence_before();
       mbar_arrive(&s_free[t]);  // S_t has been read: the MMA warp may overwrite it
       l += rs;
