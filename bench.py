@@ -136,6 +136,21 @@ def _traffic_for(kernel_class, launch_key):
     return e.get("dram_bytes_per_launch")
 
 
+def first_clip_for_rank(rank: int, batch: int) -> int:
+    """Replicas encode disjoint clips: rank r takes clip streams r*B .. r*B+B-1."""
+    return rank * batch
+
+
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The slowest rank's value (the job's time), or value itself on one rank."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def cpu_baseline(cfg, weights, clip, blocks=2):
     """The oracle, as it stands, on the host cores: one clip, patch embed + a
     few blocks timed; the full-clip time is the embed time plus the mean block
@@ -230,7 +245,7 @@ def main():
     n_tok = synth.tokens_per_clip(cfg)
     weights = synth.encoder_weights(cfg)
     # each rank encodes its own clips (clip streams rank*B .. rank*B+B-1)
-    clip_np = synth.clip_u8(cfg, batch=B, first_clip=rank * B)
+    clip_np = synth.clip_u8(cfg, batch=B, first_clip=first_clip_for_rank(rank, B))
     enc = jg.Encoder(cfg, weights, device=local)
     clip = torch.from_numpy(clip_np).cuda()
     out = torch.empty((B, n_tok, cfg.embed_dim), dtype=torch.float32, device="cuda")
@@ -260,11 +275,7 @@ def main():
         dist.barrier()
     enc.set_profiling(False)
     prof = enc.profile(reset=True)
-    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), dist, "cuda")
     ms_step = total_ms / args.steps
     tokens = world * B * n_tok * args.steps
     value = tokens / (total_ms / 1e3)
@@ -295,12 +306,8 @@ def main():
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
         enc.encode_host(hclip, hout)
-    e2e_s = (time.perf_counter() - t0) / args.e2e_steps
-    e2e_val = B * n_tok / e2e_s
-    if dist:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_val = world * B * n_tok / float(t.item())
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, dist, "cuda")
+    e2e_val = world * B * n_tok / e2e_s
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -3,19 +3,19 @@
 // One CTA owns two 128-row query tiles (Q0, Q1) of one (clip, head).  Keys
 // and values stream in tiles of 128 through a 3-deep TMA ring shared by both
 // query tiles.  For query tile t and key tile j:
-//   S_t = Q_t K_j^T     tcgen05.mma into TMEM (fp32, 128 lanes x 128 columns);
-//   softmax warpgroup t (one thread per query row) reads S_t from TMEM once
-//   (twice for the first key tile, whose row max starts the running max m),
-//   writes P_t = 2^((S_t - m) scale log2e) as 16-bit values into
-//   128B-swizzled shared memory, accumulates the row sum l in fp32 and
-//   releases the TMEM buffer;
+//   S_t = Q_t K_j^T     tcgen05.mma into one of three TMEM score buffers (fp32,
+//                       128 lanes x 128 columns) used round-robin by S0_0, S1_0,
+//                       S0_1, S1_1, ... so the scores of key tile j+1 are being
+//                       computed while both softmax warpgroups work on tile j;
+//   softmax warpgroup t (one thread per query row) reads S_t from TMEM twice
+//   (row max, then the exponentials), writes P_t = 2^((S_t - m) scale log2e)
+//   as 16-bit values into 128B-swizzled shared memory, accumulates the row sum
+//   l in fp32 and releases the score buffer;
 //   O_t += P_t V_j      tcgen05.mma into the TMEM output accumulator.
-// The MMA warp alternates between the two tiles, so the tensor core works on
-// one tile while the other tile's softmax runs.  The running max is moved
-// (O_t and l rescaled, the tile's exponentials redone) only when a row's max
-// grows by more than 2^8 in the exponent; m, l and O stay consistent, so
-// O / l is exact up to rounding.  V arrives transposed ([hd, keys], keys contiguous): every MMA
-// operand is K-major.
+// The running max m is moved (O_t and l rescaled through TMEM) only when a
+// row's max grows by more than 2^8 in the exponent; m, l and O stay
+// consistent, so O / l is exact up to rounding.  V arrives transposed ([hd,
+// keys], keys contiguous): every MMA operand is K-major.
 //
 // Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and
 // tensor-memory owner, warps 2-5 softmax of Q0, warps 6-9 softmax of Q1
@@ -30,7 +30,8 @@ constexpr int kBQ = 128;     // query rows per tile (two tiles per CTA)
 constexpr int kBKV = 128;    // keys per tile
 constexpr int kStages = 3;   // K/V ring depth
 constexpr int kThreads = 320;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O0 [256,256+HD) O1 [384,384+HD)
+constexpr uint32_t kTmemCols = 512;  // S pool [0,384), O0 [384,384+HD), O1 [448,448+HD)
+constexpr int kSBufs = 3;
 
 template <int HD>
 struct AttnSmem {
@@ -165,9 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;  // [2] per query tile
-  uint64_t* s_free = s_full + 2;          // [2]
-  uint64_t* p_full = s_free + 2;          // [2]
+  uint64_t* s_full = kv_empty + kStages;  // [kSBufs] per score buffer
+  uint64_t* s_free = s_full + kSBufs;     // [kSBufs]
+  uint64_t* p_full = s_free + kSBufs;     // [2] per query tile
   uint64_t* pv_done = p_full + 2;         // [2]
   uint64_t* mma_done = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -184,9 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 128);
       mbar_init(&pv_done[i], 1);
     }
@@ -247,50 +250,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_f16<T, kBQ, kBKV>();
       constexpr uint32_t idesc_o = idesc_f16<T, kBQ, HD>();
       bool ok = mbar_wait(q_full, 0);
-      // Per key tile j: PV0_{j-1}, S0_j, PV1_{j-1}, S1_j (the last round only
-      // PVs).  Issuing PV_t before S_t means S_t's completion also covers PV_t.
-      for (int j = 0; ok && j <= n_kv && !*abort_flag; ++j) {
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= 1) {
-            const int jp = j - 1;
-            if (!mbar_wait(&p_full[t], jp & 1)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const int stage = jp % kStages;
-            const uint32_t ap = smem_u32(sP + t * S::kPBytes);
-            const uint32_t av = smem_u32(sV + stage * S::kVBytes);
+      // Score computation k = 2 j + t (S_t of key tile j) uses buffer k % 3.
+      // Issue order: S0_0, S1_0, then per key tile j: S0_{j+1}, PV0_j,
+      // S1_{j+1}, PV1_j, so the next scores are queued before each PV waits
+      // for its softmax.
+      auto issue_s = [&](int k) -> bool {
+        const int j = k >> 1, t = k & 1, b = k % kSBufs;
+        const int stage = j % kStages;
+        if (t == 0 && !mbar_wait(&kv_full[stage], (j / kStages) & 1)) return false;
+        if (k >= kSBufs && !mbar_wait(&s_free[b], (k / kSBufs - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t aq = smem_u32(sQ + t * S::kQBytes);
+        const uint32_t ak = smem_u32(sK + stage * S::kKBytes);
 #pragma unroll
-            for (int k = 0; k < kBKV / 16; ++k) {
-              const uint32_t off = (k & 3) * 32;
-              umma_f16_ss(tmem + 256 + t * 128, smem_desc_kmajor<128>(ap + (k >> 2) * S::kPBlock + off),
-                          smem_desc_kmajor<128>(av + (k >> 2) * S::kVBlock + off), idesc_o, (jp | k) != 0);
-            }
-            umma_commit(&pv_done[t]);
-            if (t == 1) umma_commit(&kv_empty[stage]);
-          }
-          if (j < n_kv) {
-            const int stage = j % kStages;
-            if (t == 0 && !mbar_wait(&kv_full[stage], (j / kStages) & 1)) {
-              ok = false;
-              break;
-            }
-            // S_t is free once its softmax has read S_t of key tile j-1.
-            if (j >= 1 && !mbar_wait(&s_free[t], (j - 1) & 1)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t aq = smem_u32(sQ + t * S::kQBytes);
-            const uint32_t ak = smem_u32(sK + stage * S::kKBytes);
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_f16_ss(tmem + b * kBKV, smem_desc_kmajor<kQKRow>(aq + kk * 32), smem_desc_kmajor<kQKRow>(ak + kk * 32),
+                      idesc_s, kk != 0);
+        umma_commit(&s_full[b]);
+        return true;
+      };
+      auto issue_pv = [&](int j, int t) -> bool {
+        if (!mbar_wait(&p_full[t], j & 1)) return false;
+        tc_fence_after();
+        const int stage = j % kStages;
+        const uint32_t ap = smem_u32(sP + t * S::kPBytes);
+        const uint32_t av = smem_u32(sV + stage * S::kVBytes);
 #pragma unroll
-            for (int k = 0; k < HD / 16; ++k)
-              umma_f16_ss(tmem + t * kBKV, smem_desc_kmajor<kQKRow>(aq + k * 32),
-                          smem_desc_kmajor<kQKRow>(ak + k * 32), idesc_s, k != 0);
-            umma_commit(&s_full[t]);
-          }
+        for (int kk = 0; kk < kBKV / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          umma_f16_ss(tmem + 384 + t * 64, smem_desc_kmajor<128>(ap + (kk >> 2) * S::kPBlock + off),
+                      smem_desc_kmajor<128>(av + (kk >> 2) * S::kVBlock + off), idesc_o, (j | kk) != 0);
         }
+        umma_commit(&pv_done[t]);
+        if (t == 1) umma_commit(&kv_empty[stage]);  // K_j and V_j fully used
+        return true;
+      };
+      ok = ok && issue_s(0) && issue_s(1);
+      for (int j = 0; ok && j < n_kv && !*abort_flag; ++j) {
+        if (j + 1 < n_kv) ok = issue_s(2 * (j + 1));
+        ok = ok && issue_pv(j, 0);
+        if (ok && j + 1 < n_kv) ok = issue_s(2 * (j + 1) + 1);
+        ok = ok && issue_pv(j, 1);
       }
       if (!ok) {
         atomicOr(status, DEV_TIMEOUT);
@@ -305,14 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row in tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_off + t * kBKV;
-    const uint32_t tO = tmem + lane_off + 256 + t * 128;
+    const uint32_t tO = tmem + lane_off + 384 + t * 64;
     uint8_t* pb = sP + t * S::kPBytes + r * 128;
     float m = -INFINITY;  // running max of the raw scores
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const bool w_ok = mbar_wait(&s_full[t], j & 1);
+      const int k = 2 * j + t, b = k % kSBufs;
+      const uint32_t tS = tmem + lane_off + b * kBKV;
+      const bool w_ok = mbar_wait(&s_full[b], (k / kSBufs) & 1);
       // tcgen05.ld/st are warp-collective: every decision that guards them is warp-uniform.
       if (__any_sync(0xffffffffu, !w_ok || *abort_flag)) {
         ok = false;
@@ -321,23 +322,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int kvalid = n_tok - j * kBKV;   // keys of this tile inside the sequence
       const bool full_tile = kvalid >= kBKV;
-      // The first key tile fixes the running max (one extra TMEM pass); later
-      // tiles are exponentiated against the running max in a single pass.
-      if (j == 0) m = full_tile ? tile_row_max<false>(tS, kvalid) : tile_row_max<true>(tS, kvalid);
-      float neg_m = -m * scale_log2;
-      // P_t's buffer is free (and O_t stable) once PV_t of the previous key
-      // tile is done; it was issued before S_t of this tile, so this wait
-      // normally returns at once.
+      // pass 1: row max of S_t
+      const float mx = full_tile ? tile_row_max<false>(tS, kvalid) : tile_row_max<true>(tS, kvalid);
+      if (j == 0) m = mx;
+      // O_t is stable and P_t's buffer free once PV_t of the previous key tile is done.
       if (j >= 1 && !mbar_wait(&pv_done[t], (j - 1) & 1)) ok = false;
-      float xmax;
-      float rs = full_tile ? tile_exp_store<T, false, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r, xmax)
-                           : tile_exp_store<T, true, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r, xmax);
-      if (__any_sync(0xffffffffu, xmax > 8.0f)) {
-        // Rare: a row's max grew by more than 2^8 in the exponent.  Move the
-        // running max of the warp's rows to the tile max, rescale O_t and l by
-        // 2^((m_old - m_new) scale log2e) (1 for rows whose max did not grow)
-        // and redo this tile's exponentials.
-        const float mx = full_tile ? tile_row_max<false>(tS, kvalid) : tile_row_max<true>(tS, kvalid);
+      // Move the running max of the warp's rows when any grew by more than 2^8
+      // (in the exponent): O_t and l are rescaled by 2^((m_old - m_new) scale log2e).
+      if (__any_sync(0xffffffffu, j > 0 && (mx - m) * scale_log2 > 8.0f)) {
         const float m_new = fmaxf(m, mx);
         const float corr = ex2((m - m_new) * scale_log2);
         tc_fence_after();
@@ -353,12 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         l *= corr;
         m = m_new;
-        neg_m = -m * scale_log2;
-        rs = full_tile ? tile_exp_store<T, false, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r, xmax)
-                       : tile_exp_store<T, true, S::kPBlock>(tS, kvalid, scale_log2, neg_m, pb, r, xmax);
       }
+      // pass 2: P = 2^((S - m) scale log2e), 16-bit, into swizzled smem
+      float xmax;
+      const float rs = full_tile
+                           ? tile_exp_store<T, false, S::kPBlock>(tS, kvalid, scale_log2, -m * scale_log2, pb, r, xmax)
+                           : tile_exp_store<T, true, S::kPBlock>(tS, kvalid, scale_log2, -m * scale_log2, pb, r, xmax);
       tc_fence_before();
-      mbar_arrive(&s_free[t]);  // S_t has been read: the MMA warp may overwrite it
+      mbar_arrive(&s_free[b]);  // the score buffer has been read
       l += rs;
       fence_proxy_async_smem();
       tc_fence_before();

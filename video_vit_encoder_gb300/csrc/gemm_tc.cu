@@ -11,8 +11,10 @@
 // Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and
 // tensor-memory owner, warps 2-9 epilogue (warp w reads TMEM lanes
 // 32*(w%4) .. 32*(w%4)+31 and column half (w-2)/4 of the tile).
-// With more than one row tile, CTAs run in clusters of two that share each
-// weight tile: each CTA loads half of it and TMA-multicasts it to both.
+// With more than one row tile, CTAs run as pairs (clusters of two) issuing
+// M = 256 x N = BN MMAs over both CTAs' shared memory (cta_group::2): each CTA
+// loads its 128 rows of A and half of the W tile, so per SM the bytes moved
+// per flop fall by a third against a single-CTA 128 x BN tile.
 #include "epilogue.cuh"
 #include "internal.h"
 
@@ -25,10 +27,10 @@ constexpr int kBK = 64;  // 64 x 16-bit = one 128-byte swizzle row
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;   // warps 2-9
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CM>
 struct GemmSmem {
-  static constexpr uint32_t kABytes = kBM * kBK * 2;
-  static constexpr uint32_t kBBytes = BN * kBK * 2;
+  static constexpr uint32_t kABytes = kBM * kBK * 2;          // this CTA's 128 rows of A
+  static constexpr uint32_t kBBytes = (BN / CM) * kBK * 2;    // this CTA's rows of W
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; a power of two
   static constexpr size_t kBytes = 1024 /*alignment slack*/ + (size_t)STAGES * kStageBytes + 256;
@@ -128,7 +130,7 @@ template <typename T, int BN, int STAGES, int EPI, int QHD = 0, int QLAYOUT = 0,
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
                    int K, EpiParams ep, int* status) {
-  using S = GemmSmem<BN, STAGES>;
+  using S = GemmSmem<BN, STAGES, CM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -145,22 +147,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int num_n = (N + BN - 1) / BN;
   // Work units: CM vertically adjacent 128 x BN tiles (same W rows).  With a
-  // 2-CTA cluster each CTA computes one tile of the unit and TMA-multicasts
-  // its half of the shared W tile to both CTAs.
+  // CTA pair (CM = 2) the even CTA issues one M = 256 MMA per K step over both
+  // CTAs' shared memory; each CTA holds its 128 rows of A and half of the W
+  // tile and receives its 128 rows of the accumulator in its tensor memory.
   const int num_units = ((M + kBM * CM - 1) / (kBM * CM)) * num_n;
   const int num_kb = K / kBK;
   const int rank = CM == 2 ? (int)cluster_ctarank() : 0;
+  const bool leader = rank == 0;
   const int first_unit = CM == 2 ? (int)cluster_id_x() : (int)blockIdx.x;
   const int unit_stride = CM == 2 ? (int)cluster_count_x() : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CM);   // released by the MMA of every CTA that reads the stage
+      mbar_init(&full[s], 1);    // the (even) CTA's producer arrives; bytes of both CTAs complete it
+      mbar_init(&empty[s], 1);   // released by the MMA commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], kEpiThreads);
+      mbar_init(&tempty[i], CM * (kEpiThreads / 32));   // one arrival per epilogue warp of every CTA
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -169,12 +173,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, S::kTmemCols);
-    tmem_relinquish();
+    if constexpr (CM == 2) {
+      tmem_alloc_pair(tmem_slot, S::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, S::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   if constexpr (CM == 2) {
-    cluster_sync();   // the peer's barriers are initialised before any multicast signal
+    cluster_sync();   // both CTAs' barriers and tensor memory exist before any cross-CTA signal
   } else {
     __syncthreads();
   }
@@ -182,8 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (every CTA)
     if (lane == 0) {
+      const uint32_t full0 = CM == 2 ? mapa_shared(smem_u32(full), 0) : 0;  // the even CTA's full[0]
       int stage = 0;
       uint32_t phase = 0;
       long issued = 0;
@@ -196,12 +206,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             *abort_flag = 1;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
-          tma_load_2d(sA + stage * S::kABytes, &tmA, &full[stage], kb * kBK, tm * kBM);
           if constexpr (CM == 2) {
-            tma_load_2d_multicast(sB + stage * S::kBBytes + rank * (S::kBBytes / 2), &tmB, &full[stage], kb * kBK,
-                                  tn * BN + rank * (BN / 2), (uint16_t)0x3);
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * S::kStageBytes);
+            tma_load_2d_pair(sA + stage * S::kABytes, &tmA, full0 + 8 * stage, kb * kBK, tm * kBM);
+            tma_load_2d_pair(sB + stage * S::kBBytes, &tmB, full0 + 8 * stage, kb * kBK, tn * BN + rank * (BN / 2));
           } else {
+            mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
+            tma_load_2d(sA + stage * S::kABytes, &tmA, &full[stage], kb * kBK, tm * kBM);
             tma_load_2d(sB + stage * S::kBBytes, &tmB, &full[stage], kb * kBK, tn * BN);
           }
           ++issued;
@@ -211,21 +222,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // Every copy this CTA issued must land before it exits: wait (bounded)
-      // for the last min(issued, STAGES) stages.
-      const long pending = issued < STAGES ? issued : STAGES;
-      for (long i = 0; i < pending; ++i) {
-        if (--stage < 0) {
-          stage = STAGES - 1;
-          phase ^= 1;
+      // Every copy issued must land before the CTAs exit: wait (bounded) for the
+      // last min(issued, STAGES) stages.  The even CTA's barriers count the
+      // bytes of both CTAs of a pair.
+      if (leader) {
+        const long pending = issued < STAGES ? issued : STAGES;
+        for (long i = 0; i < pending; ++i) {
+          if (--stage < 0) {
+            stage = STAGES - 1;
+            phase ^= 1;
+          }
+          mbar_wait(&full[stage], phase);
         }
-        mbar_wait(&full[stage], phase);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16<T, kBM, BN>();
+    // ------------------------------------------------------------ MMA issuer (the even CTA)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_f16<T, kBM * CM, BN>();
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -252,11 +266,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = smem_u32(sB + stage * S::kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            umma_f16_ss(d_tmem, smem_desc_kmajor<128>(a0 + k * 32), smem_desc_kmajor<128>(b0 + k * 32), idesc,
-                        (kb | k) != 0);
+            if constexpr (CM == 2) {
+              umma_f16_ss_pair(d_tmem, smem_desc_kmajor<128>(a0 + k * 32), smem_desc_kmajor<128>(b0 + k * 32), idesc,
+                               (kb | k) != 0);
+            } else {
+              umma_f16_ss(d_tmem, smem_desc_kmajor<128>(a0 + k * 32), smem_desc_kmajor<128>(b0 + k * 32), idesc,
+                          (kb | k) != 0);
+            }
           }
           if constexpr (CM == 2) {
-            umma_commit_multicast(&empty[stage], (uint16_t)0x3);
+            umma_commit_pair(&empty[stage], (uint16_t)0x3);
           } else {
             umma_commit(&empty[stage]);
           }
@@ -266,20 +285,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[buf]);
+        if constexpr (CM == 2) {
+          umma_commit_pair(&tfull[buf], (uint16_t)0x3);
+        } else {
+          umma_commit(&tfull[buf]);
+        }
       }
       // Drain: no MMA may still be running when tensor memory is released.
-      umma_commit(mma_done);
+      if constexpr (CM == 2) {
+        umma_commit_pair(mma_done, (uint16_t)0x1);
+      } else {
+        umma_commit(mma_done);
+      }
       mbar_wait(mma_done, 0);
     }
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (every CTA)
     // Eight warps: warp w drains TMEM lanes 32*(w%4) .. +31 (its rows) and the
     // column half (w-2)/4 of the tile, so two warps per SM sub-partition share
     // the epilogue work and hide each other's latency.
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row_in_tile = quarter * 32 + lane;
+    const uint32_t tempty0 = CM == 2 ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
     int acc = 0;
     for (int u = first_unit; u < num_units; u += unit_stride, ++acc) {
       const int buf = acc & 1;
@@ -300,50 +328,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                row, row < M, tn * BN, half * (BN / 2));
       } else {
 #pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2) + c * 32, r);
-        tmem_wait_ld();
-        const int col0 = tn * BN + half * (BN / 2) + c * 32;
-        if (row < M && col0 < N) {
-          float v[32];
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2) + c * 32, r);
+          tmem_wait_ld();
+          const int col0 = tn * BN + half * (BN / 2) + c * 32;
+          if (row < M && col0 < N) {
+            float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          epilogue_apply<T, EPI, 32>(ep, row, col0, v);
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            epilogue_apply<T, EPI, 32>(ep, row, col0, v);
+          }
         }
       }
-      }
       tc_fence_before();
-      mbar_arrive(&tempty[buf]);
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CM == 2) {
+          mbar_arrive_cluster(tempty0 + 8 * buf);   // the even CTA's barrier
+        } else {
+          mbar_arrive(&tempty[buf]);
+        }
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CM == 2) cluster_sync();   // the pair's MMAs and epilogues are done; no signal targets an exited CTA
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, S::kTmemCols);
+    if constexpr (CM == 2) {
+      tmem_dealloc_pair(tmem_base, S::kTmemCols);
+    } else {
+      tmem_dealloc(tmem_base, S::kTmemCols);
+    }
   }
-  if constexpr (CM == 2) cluster_sync();   // no peer signal may target this CTA after it exits
 }
 
-template <typename T, int BN, int STAGES, int EPI, int QHD = 0, int QLAYOUT = 0>
+template <typename T, int BN, int STAGES, int CM, int EPI, int QHD = 0, int QLAYOUT = 0>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
-                       int* status, cudaStream_t stream, int num_sms, int cm) {
-  using S = GemmSmem<BN, STAGES>;
+                       int* status, cudaStream_t stream, int num_sms) {
+  using S = GemmSmem<BN, STAGES, CM>;
+  auto kern = gemm_tc_kernel<T, BN, STAGES, EPI, QHD, QLAYOUT, CM>;
+  static bool configured = false;  // per instantiation
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
   const int num_m = (M + kBM - 1) / kBM, num_n = (N + BN - 1) / BN;
-  if (cm == 2) {
-    auto kern = gemm_tc_kernel<T, BN, STAGES, EPI, QHD, QLAYOUT, 2>;
-    static bool configured = false;  // per instantiation
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
-    const int units = ((num_m + 1) / 2) * num_n;
-    const int clusters = units < num_sms / 2 ? units : num_sms / 2;
+  if constexpr (CM == 2) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = S::kBytes;
     cfg.stream = stream;
@@ -354,36 +390,38 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, int M, int 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // The persistent grid holds only as many pairs as can be resident at once.
+    static int resident = 0;  // per instantiation
+    if (resident == 0) {
+      cfg.gridDim = dim3(2 * (num_sms / 2));
+      if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) resident = num_sms / 2;
+    }
+    const int units = ((num_m + 1) / 2) * num_n;
+    const int clusters = units < resident ? units : resident;
+    cfg.gridDim = dim3(2 * clusters);
     return cudaLaunchKernelEx(&cfg, kern, ta, tb, M, N, K, ep, status);
+  } else {
+    const int tiles = num_m * num_n;
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    kern<<<grid, kThreads, S::kBytes, stream>>>(ta, tb, M, N, K, ep, status);
+    return cudaGetLastError();
   }
-  auto kern = gemm_tc_kernel<T, BN, STAGES, EPI, QHD, QLAYOUT, 1>;
-  static bool configured = false;  // per instantiation
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  const int tiles = num_m * num_n;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, kThreads, S::kBytes, stream>>>(ta, tb, M, N, K, ep, status);
-  return cudaGetLastError();
 }
 
-template <typename T, int BN, int STAGES>
+template <typename T, int BN, int STAGES, int CM>
 cudaError_t dispatch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
-                         const EpiParams& ep, int* status, cudaStream_t s, int sms, int cm) {
+                         const EpiParams& ep, int* status, cudaStream_t s, int sms) {
   switch (epi) {
-    case EPI_STORE: return launch_one<T, BN, STAGES, EPI_STORE>(ta, tb, M, N, K, ep, status, s, sms, cm);
-    case EPI_F32: return launch_one<T, BN, STAGES, EPI_F32>(ta, tb, M, N, K, ep, status, s, sms, cm);
-    case EPI_RESID: return launch_one<T, BN, STAGES, EPI_RESID>(ta, tb, M, N, K, ep, status, s, sms, cm);
-    case EPI_GELU: return launch_one<T, BN, STAGES, EPI_GELU>(ta, tb, M, N, K, ep, status, s, sms, cm);
+    case EPI_STORE: return launch_one<T, BN, STAGES, CM, EPI_STORE>(ta, tb, M, N, K, ep, status, s, sms);
+    case EPI_F32: return launch_one<T, BN, STAGES, CM, EPI_F32>(ta, tb, M, N, K, ep, status, s, sms);
+    case EPI_RESID: return launch_one<T, BN, STAGES, CM, EPI_RESID>(ta, tb, M, N, K, ep, status, s, sms);
+    case EPI_GELU: return launch_one<T, BN, STAGES, CM, EPI_GELU>(ta, tb, M, N, K, ep, status, s, sms);
     case EPI_QKV:
       if (ep.head_dim == 64)
-        return ep.rope.layout == 0
-                   ? launch_one<T, BN, STAGES, EPI_QKV, 64, 0>(ta, tb, M, N, K, ep, status, s, sms, cm)
-                   : launch_one<T, BN, STAGES, EPI_QKV, 64, 1>(ta, tb, M, N, K, ep, status, s, sms, cm);
-      return ep.rope.layout == 0 ? launch_one<T, BN, STAGES, EPI_QKV, 32, 0>(ta, tb, M, N, K, ep, status, s, sms, cm)
-                                 : launch_one<T, BN, STAGES, EPI_QKV, 32, 1>(ta, tb, M, N, K, ep, status, s, sms, cm);
+        return ep.rope.layout == 0 ? launch_one<T, BN, STAGES, CM, EPI_QKV, 64, 0>(ta, tb, M, N, K, ep, status, s, sms)
+                                   : launch_one<T, BN, STAGES, CM, EPI_QKV, 64, 1>(ta, tb, M, N, K, ep, status, s, sms);
+      return ep.rope.layout == 0 ? launch_one<T, BN, STAGES, CM, EPI_QKV, 32, 0>(ta, tb, M, N, K, ep, status, s, sms)
+                                 : launch_one<T, BN, STAGES, CM, EPI_QKV, 32, 1>(ta, tb, M, N, K, ep, status, s, sms);
   }
   return cudaErrorInvalidValue;
 }
@@ -392,15 +430,20 @@ template <typename T>
 cudaError_t gemm_tc_typed(int epi, const void* A, const void* W, int M, int N, int K, const EpiParams& ep,
                           int* status, cudaStream_t s, int sms) {
   const int BN = (N % 256 == 0) ? 256 : 128;
-  // Pairs of CTAs share each W tile when there are at least two row tiles.
+  // With at least two row tiles, CTA pairs run M = 256 MMAs.
   const int cm = M > kBM ? 2 : 1;
   CUtensorMap ta, tb;
   cudaError_t e = make_tmap_2d(&ta, A, sizeof(T), K, M, (size_t)K * sizeof(T), kBK, kBM);
   if (e != cudaSuccess) return e;
   e = make_tmap_2d(&tb, W, sizeof(T), K, N, (size_t)K * sizeof(T), kBK, BN / cm);
   if (e != cudaSuccess) return e;
-  if (BN == 256) return dispatch_epi<T, 256, 4>(epi, ta, tb, M, N, K, ep, status, s, sms, cm);
-  return dispatch_epi<T, 128, 6>(epi, ta, tb, M, N, K, ep, status, s, sms, cm);
+  if (cm == 2) {
+    // a CTA holds 128 rows of A and BN/2 rows of W per stage
+    if (BN == 256) return dispatch_epi<T, 256, 6, 2>(epi, ta, tb, M, N, K, ep, status, s, sms);
+    return dispatch_epi<T, 128, 8, 2>(epi, ta, tb, M, N, K, ep, status, s, sms);
+  }
+  if (BN == 256) return dispatch_epi<T, 256, 4, 1>(epi, ta, tb, M, N, K, ep, status, s, sms);
+  return dispatch_epi<T, 128, 6, 1>(epi, ta, tb, M, N, K, ep, status, s, sms);
 }
 
 }  // namespace

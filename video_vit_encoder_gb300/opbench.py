@@ -1,0 +1,77 @@
+"""Runs and times one operation of the encoder at the ViT-L/16 batch-8 shapes.
+
+    python -m video_vit_encoder_gb300.opbench OP [--reps R] [--warmup W]
+
+OP is one of attention, qkv, out_proj, ffn_up, ffn_down, layernorm.  Shapes:
+8 clips x 2048 tokens = 16384 rows, D 1024, 16 heads (head_dim 64), FFN 4096,
+bf16 operands.  Inputs are random (the values do not matter for timing).
+Prints the mean time per launch (CUDA events) and the achieved rate.  Used
+for single-kernel profiler captures (e.g. under ncu with -k and -c).
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+import torch
+
+from . import binding as jb
+from ._lib import load
+
+B, N, D, H, F = 8, 2048, 1024, 16, 4096
+M = B * N
+
+
+def _setup(op):
+    g = torch.Generator(device="cuda").manual_seed(0)
+    bf = torch.bfloat16
+
+    def rnd(*shape, scale=1.0, dtype=bf):
+        return (torch.randn(*shape, device="cuda", generator=g) * scale).to(dtype)
+
+    if op == "attention":
+        hd = D // H
+        q, k = rnd(B * H, N, hd, scale=0.5), rnd(B * H, N, hd, scale=0.5)
+        vt = rnd(B * H, hd, N)
+        out = torch.empty(B, N, D, dtype=bf, device="cuda")
+        return (lambda: jb.attention(q, k, vt, B, H, N, hd, out=out)), 4.0 * B * H * N * N * hd, "TFLOP/s"
+    if op == "layernorm":
+        x = rnd(M, D, dtype=torch.float32)
+        w, b = torch.ones(D, device="cuda"), torch.zeros(D, device="cuda")
+        y = torch.empty_like(x)
+        return (lambda: jb.layernorm_f32(x, w, b, 1e-6, out=y)), 8.0 * M * D, "GB/s"
+    shapes = {"qkv": (3 * D, D, 0), "out_proj": (D, D, 2), "ffn_up": (F, D, 3), "ffn_down": (D, F, 2)}
+    n, kdim, epi = shapes[op]
+    A = rnd(M, kdim)
+    W = rnd(n, kdim, scale=0.02)
+    bias = torch.zeros(n, device="cuda")
+    out = torch.empty(M, n, dtype=torch.float32 if epi in (1, 2) else bf, device="cuda").zero_()
+    return (lambda: jb.linear(A, W, bias, epi, out=out)), 2.0 * M * n * kdim, "TFLOP/s"
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("op", choices=["attention", "qkv", "out_proj", "ffn_up", "ffn_down", "layernorm"])
+    ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    args = ap.parse_args(argv)
+    load()
+    fn, work, unit = _setup(args.op)
+    for _ in range(args.warmup):
+        fn()
+    jb.ops_sync()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.reps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    jb.ops_sync()
+    ms = s.elapsed_time(e) / max(args.reps, 1)
+    rate = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    print(f"{args.op}: {ms * 1e3:.1f} us/launch, {rate:.1f} {unit}")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
