@@ -33,7 +33,10 @@ struct GemmSmem {
   static constexpr uint32_t kBBytes = (BN / CM) * kBK * 2;    // this CTA's rows of W
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; a power of two
-  static constexpr size_t kBytes = 1024 /*alignment slack*/ + (size_t)STAGES * kStageBytes + 256;
+  static constexpr uint32_t kEpiStage = 4096;      // per epilogue warp: 32 rows x 128 bytes
+  static constexpr uint32_t kEpiOffset = STAGES * kStageBytes;
+  static constexpr uint32_t kBarOffset = kEpiOffset + (kEpiThreads / 32) * kEpiStage;
+  static constexpr size_t kBytes = 1024 /*alignment slack*/ + kBarOffset + 256;
 };
 
 // QKV epilogue of one thread's row of a 128 x BN accumulator tile.  BN
@@ -126,21 +129,104 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
   }
 }
 
+// Epilogue of one warp for rows row0 .. row0+31 of the tile (its TMEM lanes)
+// and NCOLS columns from col0: accumulator (+ bias, activation; + the
+// residual for EPI_RESID) -> a 32 x 128-byte staging buffer in the 128B
+// swizzle -> one TMA tensor store per 128-byte column block, so global memory
+// sees whole rows instead of one row per lane.  The residual block arrives by
+// TMA into the same buffer, requested before the accumulator is read.  Rows
+// and columns outside the output are clipped by the tensor map.
+template <typename T, int EPI, int NCOLS>
+__device__ __forceinline__ void staged_epilogue(const EpiParams& ep, const CUtensorMap* tmC, uint32_t taddr, int row0,
+                                                int col0, uint8_t* buf, uint64_t* bar, uint32_t& bar_phase, int lane,
+                                                int* status) {
+  constexpr bool kF32Out = EPI == EPI_F32 || EPI == EPI_RESID;
+  constexpr int kCols = kF32Out ? 32 : 64;  // columns per 128-byte block
+  uint8_t* my_row = buf + lane * 128;
+#pragma unroll 1
+  for (int c0 = 0; c0 < NCOLS; c0 += kCols) {
+    if constexpr (EPI == EPI_RESID) {
+      if (lane == 0) {
+        bulk_wait_read_all();  // the previous block's store has left the buffer
+        mbar_arrive_expect_tx(bar, 4096);
+        tma_load_2d(buf, tmC, bar, col0 + c0, row0);
+      }
+    }
+    float v[kCols];
+#pragma unroll
+    for (int h = 0; h < kCols / 32; ++h) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c0 + h * 32, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[h * 32 + i] = __uint_as_float(r[i]);
+    }
+    if (ep.bias != nullptr) {
+      const float4* b4 = reinterpret_cast<const float4*>(ep.bias + col0 + c0);
+#pragma unroll
+      for (int i = 0; i < kCols / 4; ++i) {
+        const float4 bb = __ldg(b4 + i);
+        v[4 * i] += bb.x;
+        v[4 * i + 1] += bb.y;
+        v[4 * i + 2] += bb.z;
+        v[4 * i + 3] += bb.w;
+      }
+    }
+    if constexpr (EPI == EPI_GELU) {
+#pragma unroll
+      for (int i = 0; i < kCols; ++i) v[i] = gelu_erf(v[i]);
+    }
+    if constexpr (EPI == EPI_RESID) {
+      if (!mbar_wait(bar, bar_phase)) atomicOr(status, DEV_TIMEOUT);
+      bar_phase ^= 1;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float4* p = reinterpret_cast<float4*>(my_row + ((k ^ (lane & 7)) << 4));
+        const float4 x = *p;
+        *p = make_float4(x.x + v[4 * k], x.y + v[4 * k + 1], x.z + v[4 * k + 2], x.w + v[4 * k + 3]);
+      }
+    } else {
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        uint4 w;
+        if constexpr (kF32Out) {
+          w = make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
+                         __float_as_uint(v[4 * k + 3]));
+        } else {
+          w = make_uint4(pack2<T>(v[8 * k], v[8 * k + 1]), pack2<T>(v[8 * k + 2], v[8 * k + 3]),
+                         pack2<T>(v[8 * k + 4], v[8 * k + 5]), pack2<T>(v[8 * k + 6], v[8 * k + 7]));
+        }
+        *reinterpret_cast<uint4*>(my_row + ((k ^ (lane & 7)) << 4)) = w;
+      }
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmC, buf, col0 + c0, row0);
+      bulk_commit_group();
+    }
+  }
+}
+
 template <typename T, int BN, int STAGES, int EPI, int QHD = 0, int QLAYOUT = 0, int CM = 1>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
-                   int K, EpiParams ep, int* status) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, EpiParams ep, int* status) {
   using S = GemmSmem<BN, STAGES, CM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * S::kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * S::kStageBytes);
+  uint8_t* sEpi = smem + S::kEpiOffset;  // epilogue staging, one 4 KB buffer per epilogue warp
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOffset);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;  // [2] accumulator ready for the epilogue
   uint64_t* tempty = tfull + 2;      // [2] accumulator drained by the epilogue
   uint64_t* mma_done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* epi_bar = mma_done + 1;  // [8] residual arrivals, one per epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + kEpiThreads / 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -167,10 +253,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[i], CM * (kEpiThreads / 32));   // one arrival per epilogue warp of every CTA
     }
     mbar_init(mma_done, 1);
+    for (int i = 0; i < kEpiThreads / 32; ++i) mbar_init(&epi_bar[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if constexpr (EPI != EPI_QKV) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     if constexpr (CM == 2) {
@@ -308,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t tempty0 = CM == 2 ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
+    uint32_t epi_phase = 0;
     int acc = 0;
     for (int u = first_unit; u < num_units; u += unit_stride, ++acc) {
       const int buf = acc & 1;
@@ -327,19 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    half * (BN / 2),
                                                row, row < M, tn * BN, half * (BN / 2));
       } else {
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2) + c * 32, r);
-          tmem_wait_ld();
-          const int col0 = tn * BN + half * (BN / 2) + c * 32;
-          if (row < M && col0 < N) {
-            float v[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-            epilogue_apply<T, EPI, 32>(ep, row, col0, v);
-          }
-        }
+        staged_epilogue<T, EPI, BN / 2>(ep, &tmC,
+                                        tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2),
+                                        row - lane, tn * BN + half * (BN / 2), sEpi + (warp - 2) * S::kEpiStage,
+                                        &epi_bar[warp - 2], epi_phase, lane, status);
       }
       tc_fence_before();
       __syncwarp();
@@ -351,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (EPI != EPI_QKV && lane == 0) bulk_wait_all();  // the tile stores have completed
   }
 
   tc_fence_before();
@@ -367,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <typename T, int BN, int STAGES, int CM, int EPI, int QHD = 0, int QLAYOUT = 0>
-cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
-                       int* status, cudaStream_t stream, int num_sms) {
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, int M, int N, int K,
+                       const EpiParams& ep, int* status, cudaStream_t stream, int num_sms) {
   using S = GemmSmem<BN, STAGES, CM>;
   auto kern = gemm_tc_kernel<T, BN, STAGES, EPI, QHD, QLAYOUT, CM>;
   static bool configured = false;  // per instantiation
@@ -399,29 +480,30 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, int M, int 
     const int units = ((num_m + 1) / 2) * num_n;
     const int clusters = units < resident ? units : resident;
     cfg.gridDim = dim3(2 * clusters);
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, M, N, K, ep, status);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, M, N, K, ep, status);
   } else {
     const int tiles = num_m * num_n;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    kern<<<grid, kThreads, S::kBytes, stream>>>(ta, tb, M, N, K, ep, status);
+    kern<<<grid, kThreads, S::kBytes, stream>>>(ta, tb, tc, M, N, K, ep, status);
     return cudaGetLastError();
   }
 }
 
 template <typename T, int BN, int STAGES, int CM>
-cudaError_t dispatch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
-                         const EpiParams& ep, int* status, cudaStream_t s, int sms) {
+cudaError_t dispatch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, int M, int N,
+                         int K, const EpiParams& ep, int* status, cudaStream_t s, int sms) {
   switch (epi) {
-    case EPI_STORE: return launch_one<T, BN, STAGES, CM, EPI_STORE>(ta, tb, M, N, K, ep, status, s, sms);
-    case EPI_F32: return launch_one<T, BN, STAGES, CM, EPI_F32>(ta, tb, M, N, K, ep, status, s, sms);
-    case EPI_RESID: return launch_one<T, BN, STAGES, CM, EPI_RESID>(ta, tb, M, N, K, ep, status, s, sms);
-    case EPI_GELU: return launch_one<T, BN, STAGES, CM, EPI_GELU>(ta, tb, M, N, K, ep, status, s, sms);
+    case EPI_STORE: return launch_one<T, BN, STAGES, CM, EPI_STORE>(ta, tb, tc, M, N, K, ep, status, s, sms);
+    case EPI_F32: return launch_one<T, BN, STAGES, CM, EPI_F32>(ta, tb, tc, M, N, K, ep, status, s, sms);
+    case EPI_RESID: return launch_one<T, BN, STAGES, CM, EPI_RESID>(ta, tb, tc, M, N, K, ep, status, s, sms);
+    case EPI_GELU: return launch_one<T, BN, STAGES, CM, EPI_GELU>(ta, tb, tc, M, N, K, ep, status, s, sms);
     case EPI_QKV:
       if (ep.head_dim == 64)
-        return ep.rope.layout == 0 ? launch_one<T, BN, STAGES, CM, EPI_QKV, 64, 0>(ta, tb, M, N, K, ep, status, s, sms)
-                                   : launch_one<T, BN, STAGES, CM, EPI_QKV, 64, 1>(ta, tb, M, N, K, ep, status, s, sms);
-      return ep.rope.layout == 0 ? launch_one<T, BN, STAGES, CM, EPI_QKV, 32, 0>(ta, tb, M, N, K, ep, status, s, sms)
-                                 : launch_one<T, BN, STAGES, CM, EPI_QKV, 32, 1>(ta, tb, M, N, K, ep, status, s, sms);
+        return ep.rope.layout == 0
+                   ? launch_one<T, BN, STAGES, CM, EPI_QKV, 64, 0>(ta, tb, tc, M, N, K, ep, status, s, sms)
+                   : launch_one<T, BN, STAGES, CM, EPI_QKV, 64, 1>(ta, tb, tc, M, N, K, ep, status, s, sms);
+      return ep.rope.layout == 0 ? launch_one<T, BN, STAGES, CM, EPI_QKV, 32, 0>(ta, tb, tc, M, N, K, ep, status, s, sms)
+                                 : launch_one<T, BN, STAGES, CM, EPI_QKV, 32, 1>(ta, tb, tc, M, N, K, ep, status, s, sms);
   }
   return cudaErrorInvalidValue;
 }
@@ -437,13 +519,20 @@ cudaError_t gemm_tc_typed(int epi, const void* A, const void* W, int M, int N, i
   if (e != cudaSuccess) return e;
   e = make_tmap_2d(&tb, W, sizeof(T), K, N, (size_t)K * sizeof(T), kBK, BN / cm);
   if (e != cudaSuccess) return e;
+  // Output map for the staged epilogue: 32-row boxes of one 128-byte column block.
+  CUtensorMap tc = ta;
+  if (epi != EPI_QKV) {
+    const int ob = (epi == EPI_F32 || epi == EPI_RESID) ? 4 : (int)sizeof(T);
+    e = make_tmap_2d(&tc, ep.out, ob, N, M, (size_t)ep.ldo * ob, 128 / ob, 32);
+    if (e != cudaSuccess) return e;
+  }
   if (cm == 2) {
     // a CTA holds 128 rows of A and BN/2 rows of W per stage
-    if (BN == 256) return dispatch_epi<T, 256, 6, 2>(epi, ta, tb, M, N, K, ep, status, s, sms);
-    return dispatch_epi<T, 128, 8, 2>(epi, ta, tb, M, N, K, ep, status, s, sms);
+    if (BN == 256) return dispatch_epi<T, 256, 6, 2>(epi, ta, tb, tc, M, N, K, ep, status, s, sms);
+    return dispatch_epi<T, 128, 8, 2>(epi, ta, tb, tc, M, N, K, ep, status, s, sms);
   }
-  if (BN == 256) return dispatch_epi<T, 256, 4, 1>(epi, ta, tb, M, N, K, ep, status, s, sms);
-  return dispatch_epi<T, 128, 6, 1>(epi, ta, tb, M, N, K, ep, status, s, sms);
+  if (BN == 256) return dispatch_epi<T, 256, 4, 1>(epi, ta, tb, tc, M, N, K, ep, status, s, sms);
+  return dispatch_epi<T, 128, 6, 1>(epi, ta, tb, tc, M, N, K, ep, status, s, sms);
 }
 
 }  // namespace
