@@ -32,6 +32,9 @@ constexpr int kStages = 3;   // K/V ring depth
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;  // S pool [0,384), O0 [384,384+HD), O1 [448,448+HD)
 constexpr int kSBufs = 3;
+// Of every four exponent pairs, this many are evaluated by the FMA-pipe
+// polynomial and the rest by ex2.approx (balances the two pipes).
+constexpr int kPolyPairs = 0;
 
 template <int HD>
 struct AttnSmem {
@@ -81,23 +84,52 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// 2^x for two values on the FMA pipe (spares the special-function unit).
+// Range reduction: n = round(x) from the low mantissa bits of x + 1.5*2^23,
+// f = x - n in [-1/2, 1/2]; 2^f by a degree-3 polynomial whose coefficients
+// were fitted here by weighted least squares on Chebyshev nodes of [-1/2, 1/2]
+// (max relative error 7.5e-5, far below the 2^-9 rounding of the 16-bit P);
+// 2^n is added to the exponent field.  x is clamped at -126, where the result
+// is below every value P can still hold next to the row maximum (2^0).
+__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
+  const uint64_t magic = pk2(0x4B400000u, 0x4B400000u);          // 1.5 * 2^23
+  const uint64_t neg_magic = pk2(0xCB400000u, 0xCB400000u);
+  const uint64_t minus1 = pk2(__float_as_uint(-1.0f), __float_as_uint(-1.0f));
+  const uint64_t c3 = pk2(__float_as_uint(0.0551716648042202f), __float_as_uint(0.0551716648042202f));
+  const uint64_t c2 = pk2(__float_as_uint(0.2426111251115799f), __float_as_uint(0.2426111251115799f));
+  const uint64_t c1 = pk2(__float_as_uint(0.6932609677314758f), __float_as_uint(0.6932609677314758f));
+  const uint64_t c0 = pk2(__float_as_uint(0.9999280571937561f), __float_as_uint(0.9999280571937561f));
+  float a, b;
+  upk2(x2, a, b);
+  x2 = pk2(__float_as_uint(fmaxf(a, -126.0f)), __float_as_uint(fmaxf(b, -126.0f)));
+  const uint64_t t = add2(x2, magic);          // 1.5*2^23 + n
+  const uint64_t f = fma2(add2(t, neg_magic), minus1, x2);   // x - n
+  uint64_t p = fma2(f, c3, c2);
+  p = fma2(f, p, c1);
+  p = fma2(f, p, c0);
+  uint32_t tl, th, pl, ph;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(tl), "=r"(th) : "l"(t));
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(pl), "=r"(ph) : "l"(p));
+  return pk2(pl + (tl << 23), ph + (th << 23));
+}
+
 // Row max of one S tile (128 columns in TMEM from taddr); columns >= kvalid
 // are ignored when MASK.
 template <bool MASK>
 __device__ __forceinline__ float tile_row_max(uint32_t taddr, int kvalid) {
   float mx = -INFINITY;
+  uint32_t u[2][32];
+  tmem_ld32(taddr, u[0]);
 #pragma unroll
-  for (int c = 0; c < kBKV / 32; c += 2) {
-    uint32_t u0[32], u1[32];
-    tmem_ld32(taddr + c * 32, u0);
-    tmem_ld32(taddr + (c + 1) * 32, u1);
-    tmem_wait_ld();
+  for (int c = 0; c < kBKV / 32; ++c) {
+    tmem_wait_ld();                                              // chunk c has arrived
+    if (c + 1 < kBKV / 32) tmem_ld32(taddr + (c + 1) * 32, u[(c + 1) & 1]);  // chunk c+1 in flight
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float a = __uint_as_float(u0[i]), b = __uint_as_float(u1[i]);
+    for (int i = 0; i < 32; i += 2) {
+      float a = __uint_as_float(u[c & 1][i]), b = __uint_as_float(u[c & 1][i + 1]);
       if (MASK) {
         a = (c * 32 + i < kvalid) ? a : -INFINITY;
-        b = ((c + 1) * 32 + i < kvalid) ? b : -INFINITY;
+        b = (c * 32 + i + 1 < kvalid) ? b : -INFINITY;
       }
       mx = max3(mx, a, b);
     }
@@ -117,25 +149,34 @@ __device__ __forceinline__ float tile_exp_store(uint32_t taddr, int kvalid, floa
   const uint64_t nm2 = pk2(__float_as_uint(neg_m), __float_as_uint(neg_m));
   uint64_t rs2 = 0;  // (0.f, 0.f)
   float xm = -INFINITY;
+  uint32_t uu[2][32];
+  tmem_ld32(taddr, uu[0]);
 #pragma unroll
   for (int c = 0; c < kBKV / 32; ++c) {
-    uint32_t u[32];
-    tmem_ld32(taddr + c * 32, u);
-    tmem_wait_ld();
+    tmem_wait_ld();                                              // chunk c has arrived
+    if (c + 1 < kBKV / 32) tmem_ld32(taddr + (c + 1) * 32, uu[(c + 1) & 1]);  // chunk c+1 in flight
+    const uint32_t(&u)[32] = uu[c & 1];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       uint32_t w[4];
 #pragma unroll
       for (int i = 0; i < 8; i += 2) {
+        const uint64_t x2 = fma2(pk2(u[g * 8 + i], u[g * 8 + i + 1]), sc2, nm2);
         float x0, x1;
-        upk2(fma2(pk2(u[g * 8 + i], u[g * 8 + i + 1]), sc2, nm2), x0, x1);
+        upk2(x2, x0, x1);
         if (MASK) {
           const int col = c * 32 + g * 8 + i;
           x0 = col < kvalid ? x0 : -INFINITY;
           x1 = col + 1 < kvalid ? x1 : -INFINITY;
         }
         xm = max3(xm, x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
+        float p0, p1;
+        if (!MASK && i / 2 >= 4 - kPolyPairs) {
+          upk2(exp2_poly2(x2), p0, p1);   // this share of the pairs on the FMA pipe
+        } else {
+          p0 = ex2(x0);
+          p1 = ex2(x1);
+        }
         rs2 = add2(rs2, pk2(__float_as_uint(p0), __float_as_uint(p1)));
         w[i / 2] = pack2<T>(p0, p1);
       }
