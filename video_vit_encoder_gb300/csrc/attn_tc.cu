@@ -117,7 +117,7 @@ __device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
 // are ignored when MASK.
 template <bool MASK>
 __device__ __forceinline__ float tile_row_max(uint32_t taddr, int kvalid) {
-  float mx = -INFINITY;
+  float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
   uint32_t u[2][32];
   tmem_ld32(taddr, u[0]);
 #pragma unroll
@@ -131,24 +131,22 @@ __device__ __forceinline__ float tile_row_max(uint32_t taddr, int kvalid) {
         a = (c * 32 + i < kvalid) ? a : -INFINITY;
         b = (c * 32 + i + 1 < kvalid) ? b : -INFINITY;
       }
-      mx = max3(mx, a, b);
+      mxs[(i >> 1) & 3] = max3(mxs[(i >> 1) & 3], a, b);
     }
   }
-  return mx;
+  return fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3]));
 }
 
 // P = 2^(S scale_log2 + neg_m) for one S tile, as 16-bit values into the
 // thread's 128B-swizzled smem row pb (16-byte chunk ch of 64-column block b
-// goes to chunk ch ^ (row % 8)); returns the row sum of P (fp32) and, in
-// xmax, the largest exponent S scale_log2 + neg_m of the row (columns >=
-// kvalid excluded when MASK).
+// goes to chunk ch ^ (row % 8)); returns the row sum of P (fp32); columns >=
+// kvalid get P = 0 when MASK.
 template <typename T, bool MASK, uint32_t kPBlock>
 __device__ __forceinline__ float tile_exp_store(uint32_t taddr, int kvalid, float scale_log2, float neg_m,
-                                                uint8_t* pb, int r, float& xmax) {
+                                                uint8_t* pb, int r) {
   const uint64_t sc2 = pk2(__float_as_uint(scale_log2), __float_as_uint(scale_log2));
   const uint64_t nm2 = pk2(__float_as_uint(neg_m), __float_as_uint(neg_m));
-  uint64_t rs2 = 0;  // (0.f, 0.f)
-  float xm = -INFINITY;
+  uint64_t rs2[4] = {0, 0, 0, 0};  // four independent (0.f, 0.f) partial sums
   uint32_t uu[2][32];
   tmem_ld32(taddr, uu[0]);
 #pragma unroll
@@ -169,7 +167,6 @@ __device__ __forceinline__ float tile_exp_store(uint32_t taddr, int kvalid, floa
           x0 = col < kvalid ? x0 : -INFINITY;
           x1 = col + 1 < kvalid ? x1 : -INFINITY;
         }
-        xm = max3(xm, x0, x1);
         float p0, p1;
         if (!MASK && i / 2 >= 4 - kPolyPairs) {
           upk2(exp2_poly2(x2), p0, p1);   // this share of the pairs on the FMA pipe
@@ -177,16 +174,15 @@ __device__ __forceinline__ float tile_exp_store(uint32_t taddr, int kvalid, floa
           p0 = ex2(x0);
           p1 = ex2(x1);
         }
-        rs2 = add2(rs2, pk2(__float_as_uint(p0), __float_as_uint(p1)));
+        rs2[i / 2] = add2(rs2[i / 2], pk2(__float_as_uint(p0), __float_as_uint(p1)));
         w[i / 2] = pack2<T>(p0, p1);
       }
       const int ch = (c & 1) * 4 + g;  // 16-byte chunk within the 128-byte row of block c/2
       *reinterpret_cast<uint4*>(pb + (c >> 1) * kPBlock + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
-  xmax = xm;
   float a, b;
-  upk2(rs2, a, b);
+  upk2(add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3])), a, b);
   return a + b;
 }
 
@@ -388,10 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
       }
       // pass 2: P = 2^((S - m) scale log2e), 16-bit, into swizzled smem
-      float xmax;
       const float rs = full_tile
-                           ? tile_exp_store<T, false, S::kPBlock>(tS, kvalid, scale_log2, -m * scale_log2, pb, r, xmax)
-                           : tile_exp_store<T, true, S::kPBlock>(tS, kvalid, scale_log2, -m * scale_log2, pb, r, xmax);
+                           ? tile_exp_store<T, false, S::kPBlock>(tS, kvalid, scale_log2, -m * scale_log2, pb, r)
+                           : tile_exp_store<T, true, S::kPBlock>(tS, kvalid, scale_log2, -m * scale_log2, pb, r);
       tc_fence_before();
       mbar_arrive(&s_free[b]);  // the score buffer has been read
       l += rs;
