@@ -54,6 +54,54 @@ template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t u) {
 // Exact-erf GELU, 0.5 z (1 + erf(z / sqrt 2)).
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 
+// GELU(z) = 0.5 z (1 + erf(z / sqrt 2)) for two values at once, with erf from
+// Abramowitz & Stegun, Handbook of Mathematical Functions, eq. 7.1.28
+// (Hastings): erf(x) = 1 - (1 + a1 x + ... + a6 x^6)^-16 for x >= 0, absolute
+// error <= 3e-7, odd in x.  Uses packed f32x2 arithmetic and one approximate
+// reciprocal per value; for the 16-bit outputs of the tensor-core path (the
+// fp32 path keeps erff).
+__device__ __forceinline__ void gelu_as2(float& z0, float& z1) {
+  uint64_t z, u, p;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(z) : "f"(z0), "f"(z1));
+  const float k = 0.70710678118654752f;
+  asm("{\n\t.reg .b64 kk;\n\tmov.b64 kk, {%2, %2};\n\tmul.rn.f32x2 %0, %1, kk;\n\t}" : "=l"(u) : "l"(z), "f"(k));
+  // |x|
+  float ua, ub;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(ua), "=f"(ub) : "l"(u));
+  const float sa = ua, sb = ub;
+  ua = fabsf(ua);
+  ub = fabsf(ub);
+  asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(ua), "f"(ub));
+#define JEPA_C2(name, v) uint64_t name; asm("mov.b64 %0, {%1, %1};" : "=l"(name) : "f"(v));
+  JEPA_C2(a6, 0.0000430638f)
+  JEPA_C2(a5, 0.0002765672f)
+  JEPA_C2(a4, 0.0001520143f)
+  JEPA_C2(a3, 0.0092705272f)
+  JEPA_C2(a2, 0.0422820123f)
+  JEPA_C2(a1, 0.0705230784f)
+  JEPA_C2(one, 1.0f)
+#undef JEPA_C2
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(p) : "l"(u), "l"(a6), "l"(a5));
+  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(u), "l"(a4));
+  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(u), "l"(a3));
+  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(u), "l"(a2));
+  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(u), "l"(a1));
+  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(u), "l"(one));
+  asm("mul.rn.f32x2 %0, %0, %0;" : "+l"(p));  // ^2
+  asm("mul.rn.f32x2 %0, %0, %0;" : "+l"(p));  // ^4
+  asm("mul.rn.f32x2 %0, %0, %0;" : "+l"(p));  // ^8
+  asm("mul.rn.f32x2 %0, %0, %0;" : "+l"(p));  // ^16
+  float pa, pb;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(pa), "=f"(pb) : "l"(p));
+  float ra, rb;  // 1/p^16 (0 once p^16 overflows: erf = +-1 there)
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(ra) : "f"(pa));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rb) : "f"(pb));
+  const float ea = copysignf(1.0f - ra, sa);
+  const float eb = copysignf(1.0f - rb, sb);
+  z0 = 0.5f * z0 * (1.0f + ea);
+  z1 = 0.5f * z1 * (1.0f + eb);
+}
+
 // ----------------------------------------------------------------------------- misc PTX
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -92,14 +140,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 }
 // Waits for the phase of parity `parity` to complete.  Returns false if it
 // did not within limit_ns (the caller then records a timeout and winds down
-// instead of spinning forever).
+// instead of spinning forever).  The limit is counted on the SM clock as
+// 2 * limit_ns cycles (about the requested time at this part's 2.07 GHz
+// maximum, longer at lower clocks) and checked once every 64 polls, so the
+// poll loop itself stays short.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if ((unsigned long long)(clock64() - t0) > 2ull * limit_ns) return false;
   }
 }
 

@@ -174,7 +174,7 @@ __device__ __forceinline__ void staged_epilogue(const EpiParams& ep, const CUten
     }
     if constexpr (EPI == EPI_GELU) {
 #pragma unroll
-      for (int i = 0; i < kCols; ++i) v[i] = gelu_erf(v[i]);
+      for (int i = 0; i < kCols; i += 2) gelu_as2(v[i], v[i + 1]);
     }
     if constexpr (EPI == EPI_RESID) {
       if (!mbar_wait(bar, bar_phase)) atomicOr(status, DEV_TIMEOUT);
