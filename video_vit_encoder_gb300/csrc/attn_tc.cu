@@ -1,25 +1,29 @@
 // Tensor-core attention for sm_103a, softmax(scale q k^T) v per (clip, head).
 //
 // One CTA owns two 128-row query tiles (Q0, Q1) of one (clip, head).  Keys
-// and values stream in tiles of 128 through a 3-deep TMA ring shared by both
+// and values stream in tiles of 128 through a 4-deep TMA ring shared by both
 // query tiles.  For query tile t and key tile j:
-//   S_t = Q_t K_j^T     tcgen05.mma into one of three TMEM score buffers (fp32,
-//                       128 lanes x 128 columns) used round-robin by S0_0, S1_0,
-//                       S0_1, S1_1, ... so the scores of key tile j+1 are being
-//                       computed while both softmax warpgroups work on tile j;
-//   softmax warpgroup t (one thread per query row) reads S_t from TMEM twice
-//   (row max, then the exponentials), writes P_t = 2^((S_t - m) scale log2e)
-//   as 16-bit values into 128B-swizzled shared memory, accumulates the row sum
-//   l in fp32 and releases the score buffer;
-//   O_t += P_t V_j      tcgen05.mma into the TMEM output accumulator.
-// The running max m is moved (O_t and l rescaled through TMEM) only when a
-// row's max grows by more than 2^8 in the exponent; m, l and O stay
-// consistent, so O / l is exact up to rounding.  V arrives transposed ([hd,
-// keys], keys contiguous): every MMA operand is K-major.
+//   S_t = Q_t K_j^T     tcgen05.mma (both operands in shared memory) into the
+//                       tile's TMEM score buffer (fp32, 128 lanes x 128 columns);
+//   softmax warpgroup t (one thread per query row) reads its row of S_t into
+//   registers in one TMEM round trip and releases the buffer at once, so the
+//   scores of key tile j+1 are computed while it works; it takes the row max,
+//   writes P_t = 2^((S_t - m) scale log2e) as 16-bit pairs into the tile's
+//   TMEM P buffer and accumulates the row sum l in fp32;
+//   O_t += P_t V_j      tcgen05.mma with A = P_t read from tensor memory and
+//                       B = V_j from shared memory, into the TMEM accumulator.
+// P never touches shared memory, whose bandwidth the operand reads of the two
+// products and the TMA writes already share.  The running max m is moved (O_t
+// and l rescaled through TMEM) only when a row's max grows by more than 2^8 in
+// the exponent; m, l and O stay consistent, so O / l is exact up to rounding.
+// V arrives transposed ([hd, keys], keys contiguous): both B operands are
+// K-major.
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and
-// tensor-memory owner, warps 2-5 softmax of Q0, warps 6-9 softmax of Q1
-// (warp w owns TMEM lanes / query rows 32*(w%4) .. +31 of its tile).
+// Warp roles (384 threads, three warpgroups): warp 0 TMA producer, warp 1 MMA
+// issuer and tensor-memory owner, warps 2-3 idle; warps 4-7 softmax of Q0,
+// warps 8-11 softmax of Q1 (warp w owns TMEM lanes / query rows 32*(w%4) ..
+// +31 of its tile).  The first warpgroup hands registers to the softmax
+// warpgroups (setmaxnreg), which hold a whole 128-score row each.
 #include "internal.h"
 
 namespace jepa {
@@ -28,10 +32,17 @@ namespace {
 
 constexpr int kBQ = 128;     // query rows per tile (two tiles per CTA)
 constexpr int kBKV = 128;    // keys per tile
-constexpr int kStages = 3;   // K/V ring depth
-constexpr int kThreads = 320;
-constexpr uint32_t kTmemCols = 512;  // S pool [0,384), O0 [384,384+HD), O1 [448,448+HD)
-constexpr int kSBufs = 3;
+constexpr int kStages = 4;   // K/V ring depth
+constexpr int kThreads = 384;
+// Register split after launch (168 per thread at launch): 128 x 72 + 256 x 216
+// = 384 x 168, and per SM sub-partition one warp of each warpgroup.
+constexpr int kRegsControl = 72;
+constexpr int kRegsSoftmax = 216;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split above the launch total");
+// TMEM columns: S_t [128 t, 128 t + 128), P_t [256 + 64 t, +64) (128 16-bit
+// values per lane), O_t [384 + 64 t, +HD).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
 // Of every four exponent pairs, this many are evaluated by the FMA-pipe
 // polynomial and the rest by ex2.approx (balances the two pipes).
 constexpr int kPolyPairs = 0;
@@ -42,18 +53,12 @@ struct AttnSmem {
   static constexpr uint32_t kKBytes = kBKV * HD * 2;
   static constexpr uint32_t kVBytes = HD * kBKV * 2;   // two 64-key blocks of HD rows x 128 B
   static constexpr uint32_t kVBlock = HD * 128;
-  static constexpr uint32_t kPBytes = kBQ * kBKV * 2;  // two 64-key blocks of 128 rows x 128 B
-  static constexpr uint32_t kPBlock = kBQ * 128;
   static constexpr uint32_t kOffK = 2 * kQBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kKBytes;
-  static constexpr uint32_t kOffP = kOffV + kStages * kVBytes;
-  static constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+  static constexpr uint32_t kOffBar = kOffV + kStages * kVBytes;
   static constexpr size_t kBytes = 1024 + kOffBar + 256;
 };
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -113,20 +118,16 @@ __device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
   return pk2(pl + (tl << 23), ph + (th << 23));
 }
 
-// Row max of one S tile (128 columns in TMEM from taddr); columns >= kvalid
-// are ignored when MASK.
+// Row max of one S tile held in registers (s[c][i] = column 32 c + i);
+// columns >= kvalid are ignored when MASK.
 template <bool MASK>
-__device__ __forceinline__ float tile_row_max(uint32_t taddr, int kvalid) {
+__device__ __forceinline__ float row_max(const uint32_t (&s)[kBKV / 32][32], int kvalid) {
   float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
-  uint32_t u[2][32];
-  tmem_ld32(taddr, u[0]);
 #pragma unroll
   for (int c = 0; c < kBKV / 32; ++c) {
-    tmem_wait_ld();                                              // chunk c has arrived
-    if (c + 1 < kBKV / 32) tmem_ld32(taddr + (c + 1) * 32, u[(c + 1) & 1]);  // chunk c+1 in flight
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
-      float a = __uint_as_float(u[c & 1][i]), b = __uint_as_float(u[c & 1][i + 1]);
+      float a = __uint_as_float(s[c][i]), b = __uint_as_float(s[c][i + 1]);
       if (MASK) {
         a = (c * 32 + i < kvalid) ? a : -INFINITY;
         b = (c * 32 + i + 1 < kvalid) ? b : -INFINITY;
@@ -137,49 +138,43 @@ __device__ __forceinline__ float tile_row_max(uint32_t taddr, int kvalid) {
   return fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3]));
 }
 
-// P = 2^(S scale_log2 + neg_m) for one S tile, as 16-bit values into the
-// thread's 128B-swizzled smem row pb (16-byte chunk ch of 64-column block b
-// goes to chunk ch ^ (row % 8)); returns the row sum of P (fp32); columns >=
-// kvalid get P = 0 when MASK.
-template <typename T, bool MASK, uint32_t kPBlock>
-__device__ __forceinline__ float tile_exp_store(uint32_t taddr, int kvalid, float scale_log2, float neg_m,
-                                                uint8_t* pb, int r) {
+// P = 2^(S scale_log2 + neg_m) for one S row held in registers, as 16-bit
+// pairs (column q holds keys 2q, 2q+1) into the thread's TMEM lane from tP;
+// returns the row sum of P (fp32); columns >= kvalid get P = 0 when MASK.
+template <typename T, bool MASK>
+__device__ __forceinline__ float exp_to_tmem(const uint32_t (&s)[kBKV / 32][32], int kvalid, float scale_log2,
+                                             float neg_m, uint32_t tP) {
   const uint64_t sc2 = pk2(__float_as_uint(scale_log2), __float_as_uint(scale_log2));
   const uint64_t nm2 = pk2(__float_as_uint(neg_m), __float_as_uint(neg_m));
   uint64_t rs2[4] = {0, 0, 0, 0};  // four independent (0.f, 0.f) partial sums
-  uint32_t uu[2][32];
-  tmem_ld32(taddr, uu[0]);
 #pragma unroll
-  for (int c = 0; c < kBKV / 32; ++c) {
-    tmem_wait_ld();                                              // chunk c has arrived
-    if (c + 1 < kBKV / 32) tmem_ld32(taddr + (c + 1) * 32, uu[(c + 1) & 1]);  // chunk c+1 in flight
-    const uint32_t(&u)[32] = uu[c & 1];
+  for (int h = 0; h < 2; ++h) {
+    uint32_t w[32];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      uint32_t w[4];
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * h + cc;
 #pragma unroll
-      for (int i = 0; i < 8; i += 2) {
-        const uint64_t x2 = fma2(pk2(u[g * 8 + i], u[g * 8 + i + 1]), sc2, nm2);
+      for (int i = 0; i < 32; i += 2) {
+        const uint64_t x2 = fma2(pk2(s[c][i], s[c][i + 1]), sc2, nm2);
         float x0, x1;
         upk2(x2, x0, x1);
         if (MASK) {
-          const int col = c * 32 + g * 8 + i;
+          const int col = c * 32 + i;
           x0 = col < kvalid ? x0 : -INFINITY;
           x1 = col + 1 < kvalid ? x1 : -INFINITY;
         }
         float p0, p1;
-        if (!MASK && i / 2 >= 4 - kPolyPairs) {
+        if (!MASK && ((i >> 1) & 3) >= 4 - kPolyPairs) {
           upk2(exp2_poly2(x2), p0, p1);   // this share of the pairs on the FMA pipe
         } else {
           p0 = ex2(x0);
           p1 = ex2(x1);
         }
-        rs2[i / 2] = add2(rs2[i / 2], pk2(__float_as_uint(p0), __float_as_uint(p1)));
-        w[i / 2] = pack2<T>(p0, p1);
+        rs2[(i >> 1) & 3] = add2(rs2[(i >> 1) & 3], pk2(__float_as_uint(p0), __float_as_uint(p1)));
+        w[cc * 16 + i / 2] = pack2<T>(p0, p1);
       }
-      const int ch = (c & 1) * 4 + g;  // 16-byte chunk within the 128-byte row of block c/2
-      *reinterpret_cast<uint4*>(pb + (c >> 1) * kPBlock + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    tmem_st32(tP + h * 32, w);
   }
   float a, b;
   upk2(add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3])), a, b);
@@ -198,15 +193,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = smem + S::kOffK;
   uint8_t* sV = smem + S::kOffV;
-  uint8_t* sP = smem + S::kOffP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;  // [kSBufs] per score buffer
-  uint64_t* s_free = s_full + kSBufs;     // [kSBufs]
-  uint64_t* p_full = s_free + kSBufs;     // [2] per query tile
-  uint64_t* pv_done = p_full + 2;         // [2]
+  uint64_t* s_full = kv_empty + kStages;  // [2] per query tile: S_t computed
+  uint64_t* s_free = s_full + 2;          // [2] S_t read into registers
+  uint64_t* p_full = s_free + 2;          // [2] P_t written (and O_t rescaled)
+  uint64_t* pv_done = p_full + 2;         // [2] O_t += P_t V done
   uint64_t* mma_done = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -222,11 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int i = 0; i < kSBufs; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 128);
       mbar_init(&pv_done[i], 1);
     }
@@ -246,130 +238,136 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, 2 * S::kQBytes);
-      tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
-      tma_load_3d(sQ + S::kQBytes, &tmQ, q_full, 0, q0 + kBQ, bh);
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        if (!mbar_wait(&kv_empty[stage], phase ^ 1)) {
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_full, 2 * S::kQBytes);
+        tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
+        tma_load_3d(sQ + S::kQBytes, &tmQ, q_full, 0, q0 + kBQ, bh);
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        for (int j = 0; j < n_kv; ++j) {
+          if (!mbar_wait(&kv_empty[stage], phase ^ 1)) {
+            atomicOr(status, DEV_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[stage], S::kKBytes + S::kVBytes);
+          tma_load_3d(sK + stage * S::kKBytes, &tmK, &kv_full[stage], 0, j * kBKV, bh);
+          tma_load_3d(sV + stage * S::kVBytes, &tmV, &kv_full[stage], j * kBKV, 0, bh);
+          tma_load_3d(sV + stage * S::kVBytes + S::kVBlock, &tmV, &kv_full[stage], j * kBKV + 64, 0, bh);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        // the CTA does not exit with copies in flight
+        mbar_wait(q_full, 0);
+        const int pending = issued < kStages ? issued : kStages;
+        for (int i = 0; i < pending; ++i) {
+          if (--stage < 0) {
+            stage = kStages - 1;
+            phase ^= 1;
+          }
+          mbar_wait(&kv_full[stage], phase);
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = idesc_f16<T, kBQ, kBKV>();
+        constexpr uint32_t idesc_o = idesc_f16<T, kBQ, HD>();
+        bool ok = mbar_wait(q_full, 0);
+        // S_t of key tile j into the tile's score buffer, once the tile's
+        // softmax has read the previous scores out of it.
+        auto issue_s = [&](int j, int t) -> bool {
+          const int stage = j % kStages;
+          if (t == 0 && !mbar_wait(&kv_full[stage], (j / kStages) & 1)) return false;
+          if (j >= 1 && !mbar_wait(&s_free[t], (j - 1) & 1)) return false;
+          tc_fence_after();
+          const uint32_t aq = smem_u32(sQ + t * S::kQBytes);
+          const uint32_t ak = smem_u32(sK + stage * S::kKBytes);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_f16_ss(tmem + kColS + t * kBKV, smem_desc_kmajor<kQKRow>(aq + kk * 32),
+                        smem_desc_kmajor<kQKRow>(ak + kk * 32), idesc_s, kk != 0);
+          umma_commit(&s_full[t]);
+          return true;
+        };
+        // O_t += P_t V_j, P_t from tensor memory (8 columns per 16 keys).
+        auto issue_pv = [&](int j, int t) -> bool {
+          if (!mbar_wait(&p_full[t], j & 1)) return false;
+          tc_fence_after();
+          const int stage = j % kStages;
+          const uint32_t av = smem_u32(sV + stage * S::kVBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBKV / 16; ++kk)
+            umma_f16_ts(tmem + kColO + t * 64, tmem + kColP + t * 64 + kk * 8,
+                        smem_desc_kmajor<128>(av + (kk >> 2) * S::kVBlock + (kk & 3) * 32), idesc_o, (j | kk) != 0);
+          umma_commit(&pv_done[t]);
+          if (t == 1) umma_commit(&kv_empty[stage]);  // K_j and V_j fully used
+          return true;
+        };
+        // Order: S0_0, S1_0, then per key tile j: S0_{j+1}, S1_{j+1}, PV0_j,
+        // PV1_j, so the next scores are queued before each PV waits for its
+        // softmax.
+        ok = ok && issue_s(0, 0) && issue_s(0, 1);
+        for (int j = 0; ok && j < n_kv && !*abort_flag; ++j) {
+          if (j + 1 < n_kv) ok = issue_s(j + 1, 0) && issue_s(j + 1, 1);
+          ok = ok && issue_pv(j, 0) && issue_pv(j, 1);
+        }
+        if (!ok) {
           atomicOr(status, DEV_TIMEOUT);
           *abort_flag = 1;
-          break;
         }
-        mbar_arrive_expect_tx(&kv_full[stage], S::kKBytes + S::kVBytes);
-        tma_load_3d(sK + stage * S::kKBytes, &tmK, &kv_full[stage], 0, j * kBKV, bh);
-        tma_load_3d(sV + stage * S::kVBytes, &tmV, &kv_full[stage], j * kBKV, 0, bh);
-        tma_load_3d(sV + stage * S::kVBytes + S::kVBlock, &tmV, &kv_full[stage], j * kBKV + 64, 0, bh);
-        ++issued;
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
+        umma_commit(mma_done);
+        mbar_wait(mma_done, 0);
       }
-      mbar_wait(q_full, 0);
-      const int pending = issued < kStages ? issued : kStages;
-      for (int i = 0; i < pending; ++i) {
-        if (--stage < 0) {
-          stage = kStages - 1;
-          phase ^= 1;
-        }
-        mbar_wait(&kv_full[stage], phase);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16<T, kBQ, kBKV>();
-      constexpr uint32_t idesc_o = idesc_f16<T, kBQ, HD>();
-      bool ok = mbar_wait(q_full, 0);
-      // Score computation k = 2 j + t (S_t of key tile j) uses buffer k % 3.
-      // Issue order: S0_0, S1_0, then per key tile j: S0_{j+1}, PV0_j,
-      // S1_{j+1}, PV1_j, so the next scores are queued before each PV waits
-      // for its softmax.
-      auto issue_s = [&](int k) -> bool {
-        const int j = k >> 1, t = k & 1, b = k % kSBufs;
-        const int stage = j % kStages;
-        if (t == 0 && !mbar_wait(&kv_full[stage], (j / kStages) & 1)) return false;
-        if (k >= kSBufs && !mbar_wait(&s_free[b], (k / kSBufs - 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t aq = smem_u32(sQ + t * S::kQBytes);
-        const uint32_t ak = smem_u32(sK + stage * S::kKBytes);
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_f16_ss(tmem + b * kBKV, smem_desc_kmajor<kQKRow>(aq + kk * 32), smem_desc_kmajor<kQKRow>(ak + kk * 32),
-                      idesc_s, kk != 0);
-        umma_commit(&s_full[b]);
-        return true;
-      };
-      auto issue_pv = [&](int j, int t) -> bool {
-        if (!mbar_wait(&p_full[t], j & 1)) return false;
-        tc_fence_after();
-        const int stage = j % kStages;
-        const uint32_t ap = smem_u32(sP + t * S::kPBytes);
-        const uint32_t av = smem_u32(sV + stage * S::kVBytes);
-#pragma unroll
-        for (int kk = 0; kk < kBKV / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          umma_f16_ss(tmem + 384 + t * 64, smem_desc_kmajor<128>(ap + (kk >> 2) * S::kPBlock + off),
-                      smem_desc_kmajor<128>(av + (kk >> 2) * S::kVBlock + off), idesc_o, (j | kk) != 0);
-        }
-        umma_commit(&pv_done[t]);
-        if (t == 1) umma_commit(&kv_empty[stage]);  // K_j and V_j fully used
-        return true;
-      };
-      ok = ok && issue_s(0) && issue_s(1);
-      for (int j = 0; ok && j < n_kv && !*abort_flag; ++j) {
-        if (j + 1 < n_kv) ok = issue_s(2 * (j + 1));
-        ok = ok && issue_pv(j, 0);
-        if (ok && j + 1 < n_kv) ok = issue_s(2 * (j + 1) + 1);
-        ok = ok && issue_pv(j, 1);
-      }
-      if (!ok) {
-        atomicOr(status, DEV_TIMEOUT);
-        *abort_flag = 1;
-      }
-      umma_commit(mma_done);
-      mbar_wait(mma_done, 0);
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax + output (tile t)
-    const int t = (warp - 2) >> 2;
+    const int t = (warp - 4) >> 2;
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // row in tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tO = tmem + lane_off + 384 + t * 64;
-    uint8_t* pb = sP + t * S::kPBytes + r * 128;
+    const uint32_t tS = tmem + lane_off + kColS + t * kBKV;
+    const uint32_t tP = tmem + lane_off + kColP + t * 64;
+    const uint32_t tO = tmem + lane_off + kColO + t * 64;
     float m = -INFINITY;  // running max of the raw scores
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const int k = 2 * j + t, b = k % kSBufs;
-      const uint32_t tS = tmem + lane_off + b * kBKV;
-      const bool w_ok = mbar_wait(&s_full[b], (k / kSBufs) & 1);
+      const bool w_ok = mbar_wait(&s_full[t], j & 1);
       // tcgen05.ld/st are warp-collective: every decision that guards them is warp-uniform.
       if (__any_sync(0xffffffffu, !w_ok || *abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // the whole score row into registers in one TMEM round trip; the
+      // buffer is released at once so the next scores can be computed into it
+      uint32_t sv[kBKV / 32][32];
+#pragma unroll
+      for (int c = 0; c < kBKV / 32; ++c) tmem_ld32(tS + c * 32, sv[c]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s_free[t]);
       const int kvalid = n_tok - j * kBKV;   // keys of this tile inside the sequence
       const bool full_tile = kvalid >= kBKV;
-      // pass 1: row max of S_t
-      const float mx = full_tile ? tile_row_max<false>(tS, kvalid) : tile_row_max<true>(tS, kvalid);
+      const float mx = full_tile ? row_max<false>(sv, kvalid) : row_max<true>(sv, kvalid);
       if (j == 0) m = mx;
       // O_t is stable and P_t's buffer free once PV_t of the previous key tile is done.
       if (j >= 1 && !mbar_wait(&pv_done[t], (j - 1) & 1)) ok = false;
+      tc_fence_after();
       // Move the running max of the warp's rows when any grew by more than 2^8
       // (in the exponent): O_t and l are rescaled by 2^((m_old - m_new) scale log2e).
       if (__any_sync(0xffffffffu, j > 0 && (mx - m) * scale_log2 > 8.0f)) {
         const float m_new = fmaxf(m, mx);
         const float corr = ex2((m - m_new) * scale_log2);
-        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t u[32];
@@ -379,18 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * corr);
           tmem_st32(tO + c * 32, u);
         }
-        tmem_wait_st();
         l *= corr;
         m = m_new;
       }
-      // pass 2: P = 2^((S - m) scale log2e), 16-bit, into swizzled smem
-      const float rs = full_tile
-                           ? tile_exp_store<T, false, S::kPBlock>(tS, kvalid, scale_log2, -m * scale_log2, pb, r)
-                           : tile_exp_store<T, true, S::kPBlock>(tS, kvalid, scale_log2, -m * scale_log2, pb, r);
-      tc_fence_before();
-      mbar_arrive(&s_free[b]);  // the score buffer has been read
+      // P = 2^((S - m) scale log2e), 16-bit, into tensor memory
+      const float rs = full_tile ? exp_to_tmem<T, false>(sv, kvalid, scale_log2, -m * scale_log2, tP)
+                                 : exp_to_tmem<T, true>(sv, kvalid, scale_log2, -m * scale_log2, tP);
       l += rs;
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[t]);
       if (__any_sync(0xffffffffu, !ok)) break;
@@ -401,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
     } else {
       tc_fence_after();
-      const int row = q0 + t * kBQ + r;
+      const int row = q0 + t * kBQ + quarter * 32 + lane;
       const float inv = 1.0f / l;
       const int b = bh / n_head, head = bh - (bh / n_head) * n_head;
       T* op = out + ((size_t)b * n_tok + row) * (size_t)(n_head * HD) + head * HD;
@@ -450,6 +444,12 @@ cudaError_t launch_t(const void* q, const void* k, const void* vt, void* out, in
   if (!configured) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
     if (e != cudaSuccess) return e;
+    // setmaxnreg.inc waits until the registers it asks for are free within the
+    // block's launch allocation: refuse to launch when the allocation is short.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kThreads < 128 * kRegsControl + 256 * kRegsSoftmax) return cudaErrorInvalidConfiguration;
     configured = true;
   }
   dim3 grid((n_tok + 2 * kBQ - 1) / (2 * kBQ), (unsigned)BH);
