@@ -278,55 +278,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t idesc_s = idesc_f16<T, kBQ, kBKV>();
-        constexpr uint32_t idesc_o = idesc_f16<T, kBQ, HD>();
-        bool ok = mbar_wait(q_full, 0);
-        // S_t of key tile j into the tile's score buffer, once the tile's
-        // softmax has read the previous scores out of it.
-        auto issue_s = [&](int j, int t) -> bool {
-          const int stage = j % kStages;
-          if (t == 0 && !mbar_wait(&kv_full[stage], (j / kStages) & 1)) return false;
-          if (j >= 1 && !mbar_wait(&s_free[t], (j - 1) & 1)) return false;
-          tc_fence_after();
-          const uint32_t aq = smem_u32(sQ + t * S::kQBytes);
-          const uint32_t ak = smem_u32(sK + stage * S::kKBytes);
+      // The whole warp walks the schedule (waits are warp-uniform); one
+      // elected lane issues each MMA and commit.
+      constexpr uint32_t idesc_s = idesc_f16<T, kBQ, kBKV>();
+      constexpr uint32_t idesc_o = idesc_f16<T, kBQ, HD>();
+      bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0));
+      // S_t of key tile j into the tile's score buffer, once the tile's
+      // softmax has read the previous scores out of it.
+      auto issue_s = [&](int j, int t) -> bool {
+        const int stage = j % kStages;
+        if (t == 0 && !__all_sync(0xffffffffu, mbar_wait(&kv_full[stage], (j / kStages) & 1))) return false;
+        if (j >= 1 && !__all_sync(0xffffffffu, mbar_wait(&s_free[t], (j - 1) & 1))) return false;
+        tc_fence_after();
+        const uint64_t dq = smem_desc_kmajor<kQKRow>(smem_u32(sQ + t * S::kQBytes));
+        const uint64_t dk = smem_desc_kmajor<kQKRow>(smem_u32(sK + stage * S::kKBytes));
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk)
-            umma_f16_ss(tmem + kColS + t * kBKV, smem_desc_kmajor<kQKRow>(aq + kk * 32),
-                        smem_desc_kmajor<kQKRow>(ak + kk * 32), idesc_s, kk != 0);
-          umma_commit(&s_full[t]);
-          return true;
-        };
-        // O_t += P_t V_j, P_t from tensor memory (8 columns per 16 keys).
-        auto issue_pv = [&](int j, int t) -> bool {
-          if (!mbar_wait(&p_full[t], j & 1)) return false;
-          tc_fence_after();
-          const int stage = j % kStages;
-          const uint32_t av = smem_u32(sV + stage * S::kVBytes);
+        for (int kk = 0; kk < HD / 16; ++kk)  // +32 bytes along K = +2 in the descriptor's address field
+          umma_f16_ss_warp(tmem + kColS + t * kBKV, dq + kk * 2, dk + kk * 2, idesc_s, kk != 0);
+        umma_commit_warp(&s_full[t]);
+        return true;
+      };
+      // O_t += P_t V_j, P_t from tensor memory (8 columns per 16 keys).
+      auto issue_pv = [&](int j, int t) -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait(&p_full[t], j & 1))) return false;
+        tc_fence_after();
+        const int stage = j % kStages;
+        const uint64_t dv = smem_desc_kmajor<128>(smem_u32(sV + stage * S::kVBytes));
 #pragma unroll
-          for (int kk = 0; kk < kBKV / 16; ++kk)
-            umma_f16_ts(tmem + kColO + t * 64, tmem + kColP + t * 64 + kk * 8,
-                        smem_desc_kmajor<128>(av + (kk >> 2) * S::kVBlock + (kk & 3) * 32), idesc_o, (j | kk) != 0);
-          umma_commit(&pv_done[t]);
-          if (t == 1) umma_commit(&kv_empty[stage]);  // K_j and V_j fully used
-          return true;
-        };
-        // Order: S0_0, S1_0, then per key tile j: S0_{j+1}, S1_{j+1}, PV0_j,
-        // PV1_j, so the next scores are queued before each PV waits for its
-        // softmax.
-        ok = ok && issue_s(0, 0) && issue_s(0, 1);
-        for (int j = 0; ok && j < n_kv && !*abort_flag; ++j) {
-          if (j + 1 < n_kv) ok = issue_s(j + 1, 0) && issue_s(j + 1, 1);
-          ok = ok && issue_pv(j, 0) && issue_pv(j, 1);
-        }
-        if (!ok) {
-          atomicOr(status, DEV_TIMEOUT);
-          *abort_flag = 1;
-        }
-        umma_commit(mma_done);
-        mbar_wait(mma_done, 0);
+        for (int kk = 0; kk < kBKV / 16; ++kk)
+          umma_f16_ts_warp(tmem + kColO + t * 64, tmem + kColP + t * 64 + kk * 8,
+                           dv + (kk >> 2) * (S::kVBlock >> 4) + (kk & 3) * 2, idesc_o, (j | kk) != 0);
+        umma_commit_warp(&pv_done[t]);
+        if (t == 1) umma_commit_warp(&kv_empty[stage]);  // K_j and V_j fully used
+        return true;
+      };
+      // Order: S0_0, S1_0, then per key tile j: S0_{j+1}, S1_{j+1}, PV0_j,
+      // PV1_j, so the next scores are queued before each PV waits for its
+      // softmax.
+      ok = ok && issue_s(0, 0) && issue_s(0, 1);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (__any_sync(0xffffffffu, *abort_flag)) break;
+        if (j + 1 < n_kv) ok = issue_s(j + 1, 0) && issue_s(j + 1, 1);
+        ok = ok && issue_pv(j, 0) && issue_pv(j, 1);
       }
+      if (!ok && lane == 0) {
+        atomicOr(status, DEV_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit_warp(mma_done);
+      mbar_wait(mma_done, 0);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));

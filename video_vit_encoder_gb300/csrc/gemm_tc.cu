@@ -326,46 +326,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (the even CTA)
-    if (lane == 0 && leader) {
+    // The whole warp walks the schedule (waits are warp-uniform); one elected
+    // lane issues each MMA and commit.
+    if (leader) {
       constexpr uint32_t idesc = idesc_f16<T, kBM * CM, BN>();
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
-      for (int u = first_unit; u < num_units && !*abort_flag; u += unit_stride, ++acc) {
+      bool ok = true;
+      for (int u = first_unit; u < num_units; u += unit_stride, ++acc) {
+        if (__any_sync(0xffffffffu, *abort_flag)) break;
         const int buf = acc & 1;
         const uint32_t acc_phase = (acc >> 1) & 1;
-        if (!mbar_wait(&tempty[buf], acc_phase ^ 1)) {
-          atomicOr(status, DEV_TIMEOUT);
-          *abort_flag = 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&tempty[buf], acc_phase ^ 1))) {
+          ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN;
-        bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase)) {
-            atomicOr(status, DEV_TIMEOUT);
-            *abort_flag = 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * S::kABytes);
-          const uint32_t b0 = smem_u32(sB + stage * S::kBBytes);
+          const uint64_t da = smem_desc_kmajor<128>(smem_u32(sA + stage * S::kABytes));
+          const uint64_t db = smem_desc_kmajor<128>(smem_u32(sB + stage * S::kBBytes));
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
+          for (int k = 0; k < kBK / 16; ++k) {  // +32 bytes along K = +2 in the descriptor's address field
             if constexpr (CM == 2) {
-              umma_f16_ss_pair(d_tmem, smem_desc_kmajor<128>(a0 + k * 32), smem_desc_kmajor<128>(b0 + k * 32), idesc,
-                               (kb | k) != 0);
+              umma_f16_ss_pair_warp(d_tmem, da + k * 2, db + k * 2, idesc, (kb | k) != 0);
             } else {
-              umma_f16_ss(d_tmem, smem_desc_kmajor<128>(a0 + k * 32), smem_desc_kmajor<128>(b0 + k * 32), idesc,
-                          (kb | k) != 0);
+              umma_f16_ss_warp(d_tmem, da + k * 2, db + k * 2, idesc, (kb | k) != 0);
             }
           }
           if constexpr (CM == 2) {
-            umma_commit_pair(&empty[stage], (uint16_t)0x3);
+            umma_commit_pair_warp(&empty[stage], (uint16_t)0x3);
           } else {
-            umma_commit(&empty[stage]);
+            umma_commit_warp(&empty[stage]);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -374,16 +372,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         if constexpr (CM == 2) {
-          umma_commit_pair(&tfull[buf], (uint16_t)0x3);
+          umma_commit_pair_warp(&tfull[buf], (uint16_t)0x3);
         } else {
-          umma_commit(&tfull[buf]);
+          umma_commit_warp(&tfull[buf]);
         }
+      }
+      if (!ok && lane == 0) {
+        atomicOr(status, DEV_TIMEOUT);
+        *abort_flag = 1;
       }
       // Drain: no MMA may still be running when tensor memory is released.
       if constexpr (CM == 2) {
-        umma_commit_pair(mma_done, (uint16_t)0x1);
+        umma_commit_pair_warp(mma_done, (uint16_t)0x1);
       } else {
-        umma_commit(mma_done);
+        umma_commit_warp(mma_done);
       }
       mbar_wait(mma_done, 0);
     }
