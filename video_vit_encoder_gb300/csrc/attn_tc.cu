@@ -19,10 +19,12 @@
 // V arrives transposed ([hd, keys], keys contiguous): both B operands are
 // K-major.
 //
-// Warp roles (384 threads, three warpgroups): warp 0 TMA producer, warp 1 MMA
-// issuer and tensor-memory owner, warps 2-3 idle; warps 4-7 softmax of Q0,
-// warps 8-11 softmax of Q1 (warp w owns TMEM lanes / query rows 32*(w%4) ..
-// +31 of its tile).  The first warpgroup hands registers to the softmax
+// Warp roles (384 threads, three warpgroups): warp 0 TMA producer, warp 1
+// MMA issuer of Q0 and tensor-memory owner, warp 2 MMA issuer of Q1, warp 3
+// idle; warps 4-7 softmax of Q0, warps 8-11 softmax of Q1 (warp w owns TMEM
+// lanes / query rows 32*(w%4) .. +31 of its tile).  One issuer per query tile
+// keeps each issuer's chain of waits and issues short: every SM
+// sub-partition also runs two softmax warps.  The first warpgroup hands registers to the softmax
 // warpgroups (setmaxnreg), which hold a whole 128-score row each.
 #include "internal.h"
 
@@ -201,8 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_free = s_full + 2;          // [2] S_t read into registers
   uint64_t* p_full = s_free + 2;          // [2] P_t written (and O_t rescaled)
   uint64_t* pv_done = p_full + 2;         // [2] O_t += P_t V done
-  uint64_t* mma_done = pv_done + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* mma_done = pv_done + 2;      // [2] per issuer
+  uint64_t* exp_tok = mma_done + 2;      // [2][4] exponential phase of tile t done, per TMEM quarter
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(exp_tok + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&kv_empty[s], 2);  // both query tiles' issuers
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -222,7 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_full[i], 128);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&exp_tok[i], 32);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -276,57 +281,58 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&kv_full[stage], phase);
         }
       }
-    } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 2) {
+      // ------------------------------------------------------------ MMA issuer of query tile t
       // The whole warp walks the schedule (waits are warp-uniform); one
       // elected lane issues each MMA and commit.
+      const int t = warp - 1;
       constexpr uint32_t idesc_s = idesc_f16<T, kBQ, kBKV>();
       constexpr uint32_t idesc_o = idesc_f16<T, kBQ, HD>();
+      const uint64_t dq = smem_desc_kmajor<kQKRow>(smem_u32(sQ + t * S::kQBytes));
+      const uint32_t dS = tmem + kColS + t * kBKV, dP = tmem + kColP + t * 64, dO = tmem + kColO + t * 64;
       bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0));
       // S_t of key tile j into the tile's score buffer, once the tile's
       // softmax has read the previous scores out of it.
-      auto issue_s = [&](int j, int t) -> bool {
+      auto issue_s = [&](int j) -> bool {
         const int stage = j % kStages;
-        if (t == 0 && !__all_sync(0xffffffffu, mbar_wait(&kv_full[stage], (j / kStages) & 1))) return false;
+        if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[stage], (j / kStages) & 1))) return false;
         if (j >= 1 && !__all_sync(0xffffffffu, mbar_wait(&s_free[t], (j - 1) & 1))) return false;
         tc_fence_after();
-        const uint64_t dq = smem_desc_kmajor<kQKRow>(smem_u32(sQ + t * S::kQBytes));
         const uint64_t dk = smem_desc_kmajor<kQKRow>(smem_u32(sK + stage * S::kKBytes));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)  // +32 bytes along K = +2 in the descriptor's address field
-          umma_f16_ss_warp(tmem + kColS + t * kBKV, dq + kk * 2, dk + kk * 2, idesc_s, kk != 0);
+          umma_f16_ss_warp(dS, dq + kk * 2, dk + kk * 2, idesc_s, kk != 0);
         umma_commit_warp(&s_full[t]);
         return true;
       };
       // O_t += P_t V_j, P_t from tensor memory (8 columns per 16 keys).
-      auto issue_pv = [&](int j, int t) -> bool {
+      auto issue_pv = [&](int j) -> bool {
         if (!__all_sync(0xffffffffu, mbar_wait(&p_full[t], j & 1))) return false;
         tc_fence_after();
         const int stage = j % kStages;
         const uint64_t dv = smem_desc_kmajor<128>(smem_u32(sV + stage * S::kVBytes));
 #pragma unroll
         for (int kk = 0; kk < kBKV / 16; ++kk)
-          umma_f16_ts_warp(tmem + kColO + t * 64, tmem + kColP + t * 64 + kk * 8,
-                           dv + (kk >> 2) * (S::kVBlock >> 4) + (kk & 3) * 2, idesc_o, (j | kk) != 0);
+          umma_f16_ts_warp(dO, dP + kk * 8, dv + (kk >> 2) * (S::kVBlock >> 4) + (kk & 3) * 2, idesc_o,
+                           (j | kk) != 0);
         umma_commit_warp(&pv_done[t]);
-        if (t == 1) umma_commit_warp(&kv_empty[stage]);  // K_j and V_j fully used
+        umma_commit_warp(&kv_empty[stage]);  // this tile is done with K_j and V_j
         return true;
       };
-      // Order: S0_0, S1_0, then per key tile j: S0_{j+1}, S1_{j+1}, PV0_j,
-      // PV1_j, so the next scores are queued before each PV waits for its
-      // softmax.
-      ok = ok && issue_s(0, 0) && issue_s(0, 1);
+      // Order: S_0, then per key tile j: S_{j+1}, PV_j, so the next scores
+      // are queued before PV_j waits for the softmax.
+      ok = ok && issue_s(0);
       for (int j = 0; ok && j < n_kv; ++j) {
         if (__any_sync(0xffffffffu, *abort_flag)) break;
-        if (j + 1 < n_kv) ok = issue_s(j + 1, 0) && issue_s(j + 1, 1);
-        ok = ok && issue_pv(j, 0) && issue_pv(j, 1);
+        if (j + 1 < n_kv) ok = issue_s(j + 1);
+        ok = ok && issue_pv(j);
       }
       if (!ok && lane == 0) {
         atomicOr(status, DEV_TIMEOUT);
         *abort_flag = 1;
       }
-      umma_commit_warp(mma_done);
-      mbar_wait(mma_done, 0);
+      umma_commit_warp(&mma_done[t]);
+      mbar_wait(&mma_done[t], 0);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
@@ -380,10 +386,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= corr;
         m = m_new;
       }
+      // The two tiles' warps on one SM sub-partition take turns at the
+      // exponentials (Q0 of key tile j, Q1 of j, Q0 of j+1, ...), so one
+      // tile's TMEM load and row max overlap the other's special-function
+      // work instead of both contending for it at once.
+      if (t == 1 || j >= 1) {
+        const bool tok_ok = mbar_wait(&exp_tok[(1 - t) * 4 + quarter], (t == 0 ? j - 1 : j) & 1);
+        if (!tok_ok) ok = false;
+      }
       // P = 2^((S - m) scale log2e), 16-bit, into tensor memory
       const float rs = full_tile ? exp_to_tmem<T, false>(sv, kvalid, scale_log2, -m * scale_log2, tP)
                                  : exp_to_tmem<T, true>(sv, kvalid, scale_log2, -m * scale_log2, tP);
       l += rs;
+      mbar_arrive(&exp_tok[t * 4 + quarter]);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[t]);
