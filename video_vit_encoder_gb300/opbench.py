@@ -2,7 +2,9 @@
 
     python -m video_vit_encoder_gb300.opbench OP [--reps R] [--warmup W]
 
-OP is one of attention, qkv, out_proj, ffn_up, ffn_down, layernorm.  Shapes:
+OP is one of attention, qkv, out_proj, ffn_up, ffn_down, layernorm, and
+out_proj_f32 / out_proj_bf16 (the out_proj shape with a plain fp32 or 16-bit
+store instead of the residual add).  Shapes:
 8 clips x 2048 tokens = 16384 rows, D 1024, 16 heads (head_dim 64), FFN 4096,
 bf16 operands.  Inputs are random (the values do not matter for timing).
 Prints the mean time per launch (CUDA events) and the achieved rate.  Used
@@ -40,7 +42,8 @@ def _setup(op):
         w, b = torch.ones(D, device="cuda"), torch.zeros(D, device="cuda")
         y = torch.empty_like(x)
         return (lambda: jb.layernorm_f32(x, w, b, 1e-6, out=y)), 8.0 * M * D, "GB/s"
-    shapes = {"qkv": (3 * D, D, 0), "out_proj": (D, D, 2), "ffn_up": (F, D, 3), "ffn_down": (D, F, 2)}
+    shapes = {"qkv": (3 * D, D, 0), "out_proj": (D, D, 2), "ffn_up": (F, D, 3), "ffn_down": (D, F, 2),
+              "out_proj_f32": (D, D, 1), "out_proj_bf16": (D, D, 0)}
     n, kdim, epi = shapes[op]
     A = rnd(M, kdim)
     W = rnd(n, kdim, scale=0.02)
@@ -51,7 +54,8 @@ def _setup(op):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["attention", "qkv", "out_proj", "ffn_up", "ffn_down", "layernorm"])
+    ap.add_argument("op", choices=["attention", "qkv", "out_proj", "ffn_up", "ffn_down", "layernorm", "out_proj_f32",
+                                   "out_proj_bf16"])
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args(argv)
