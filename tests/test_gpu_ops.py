@@ -136,6 +136,25 @@ def test_attention_tc(jg, dtype, hd, N, logit_std):
     assert_close_16bit(got, ref, f"attention {dtype} hd{hd} N{N}")
 
 
+@pytest.mark.parametrize("N,hd", [(2048, 64), (8192, 64), (8192, 32), (18432, 64)])
+@pytest.mark.parametrize("logit_std", [1.0, 4.0])
+def test_attention_tc_long_sampled_rows(jg, N, hd, logit_std):
+    """The sequence lengths of the ViT-L 16-frame 256 px clip (2048), the
+    64-frame 256 px clip with its hd-32 predictor (8192) and the 64-frame
+    384 px clip (18 432), bf16.  Sampled query rows are checked against the
+    oracle over all keys.  Planted outliers put one row's largest logit in
+    the first key tile and another's in the last key tile."""
+    B, H, dtype = 1, 2, "bf16"
+    rng = np.random.default_rng(N * 7 + hd + int(logit_std))
+    q, k, v = _attn_inputs(rng, B, H, N, hd, dtype, logit_std)
+    k[:, 11] = synth.round_to_dtype(q[:, 5] * 3, dtype)
+    k[:, N - 3] = synth.round_to_dtype(q[:, N // 2] * 3, dtype)
+    got = _run_attn(jg, q, k, v, B, H, N, hd, dtype).reshape(N, H, hd)
+    rows = np.unique(np.concatenate([[0, 5, N // 2, N - 1], rng.choice(N, 60, replace=False)]))
+    ref = oracle.attention_heads(q[:, rows], k, v)                  # [H, rows, hd]
+    assert_close_16bit(got[rows].transpose(1, 0, 2), ref, f"attention N{N} hd{hd} std{logit_std}")
+
+
 @pytest.mark.parametrize("hd,N", [(64, 130), (32, 77)])
 def test_attention_f32(jg, hd, N):
     B, H = 1, 2
