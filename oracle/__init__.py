@@ -13,5 +13,5 @@ from .encoder import (  # noqa: F401
     normalise_clip, patch_embed, token_positions, rope_split, rope_tables,
     rot90_pairs, apply_rope, layer_norm, gelu_erf, attention_heads,
     block_forward, block_forward_rows, encoder_forward, predictor_forward,
-    grid_positions_from_ids, predictor_input, encoder_rope, encoder_embed,
+    grid_positions_from_ids, predictor_input, encoder_rope, encoder_embed, is_image,
 )

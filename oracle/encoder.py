@@ -254,14 +254,32 @@ def block_forward_rows(x, wts, layer: int, n_head: int, eps: float, COS, SIN, ro
 
 
 # ----------------------------------------------------------------------------- encoder
+def is_image(cfg, T: int) -> bool:
+    """[N] §3 (2.1 encoder forward): a one-frame input takes the native image
+    path (tubelet 1, patch_embed_img, mod_embed_img); Meta's code selects it by
+    the frame count.  Models without that path (V-JEPA 2) take clips only."""
+    return T == 1 and bool(getattr(cfg, "has_image_path", False))
+
+
 def encoder_rope(cfg, T: int, H: int, W: int):
-    gt, gh, gw = T // cfg.tubelet, H // cfg.patch, W // cfg.patch
+    tub = 1 if is_image(cfg, T) else cfg.tubelet
+    gt, gh, gw = T // tub, H // cfg.patch, W // cfg.patch
     pos = token_positions(gt, gh, gw, cfg.rope_interpolate, cfg.rope_ref_grid)
     return rope_tables(pos, cfg.embed_dim // cfg.n_head, cfg.rope_layout, cfg.rope_theta)
 
 
 def encoder_embed(cfg, wts, clip_u8):
-    """Patch embedding (+ the 2.1 video modality vector, [N] §3) of one clip."""
+    """Patch embedding (+ the 2.1 modality vector, [N] §3) of one clip, or of
+    one image ``[1, H, W, 3]`` on the native image path: tubelet 1 with
+    ``patch_embed_img`` (Conv3d weight ``[D, 3, 1, 16, 16]``, feature order
+    c*256 + y*16 + x) and ``mod_embed_img`` ([N] §2 key map, §3)."""
+    T = clip_u8.shape[0]
+    if is_image(cfg, T):
+        x = patch_embed(normalise_clip(clip_u8), wts["patch_embed_img.weight"], wts["patch_embed_img.bias"],
+                        1, cfg.patch)
+        if getattr(cfg, "has_mod_embed", False):
+            x = x + np.asarray(wts["mod_embed_img"], F64)
+        return x
     x = patch_embed(normalise_clip(clip_u8), wts["patch_embed.weight"], wts["patch_embed.bias"],
                     cfg.tubelet, cfg.patch)
     if getattr(cfg, "has_mod_embed", False):

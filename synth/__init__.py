@@ -156,6 +156,10 @@ def tensor_names_encoder(cfg: EncoderConfig):
     out += [("norm.weight", (D,), "one"), ("norm.bias", (D,), "zero")]
     for k in range(len(cfg.hier_layers)):
         out += [(f"hier_norm.{k}.weight", (D,), "one"), (f"hier_norm.{k}.bias", (D,), "zero")]
+    if cfg.has_image_path:      # appended last, so no other tensor's stream moves
+        out += [("patch_embed_img.weight", (D, 3 * cfg.patch * cfg.patch), "mat"), ("patch_embed_img.bias", (D,), "zero")]
+        if cfg.has_mod_embed:
+            out.append(("mod_embed_img", (D,), "vec"))
     return out
 
 

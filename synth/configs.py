@@ -49,6 +49,7 @@ class EncoderConfig:
     rope_ref_grid: int = 16
     hier_layers: tuple = ()
     has_mod_embed: bool = False
+    has_image_path: bool = False  # 2.1 native image path: patch_embed_img (+ mod_embed_img) for 1-frame input
     patch: int = 16
     tubelet: int = 2
     ln_eps: float = 1e-6
@@ -60,7 +61,8 @@ class EncoderConfig:
         return self.embed_dim // self.n_head
 
     def grid(self):
-        return (self.n_frames // self.tubelet, self.height // self.patch, self.width // self.patch)
+        tub = 1 if (self.n_frames == 1 and self.has_image_path) else self.tubelet
+        return (self.n_frames // tub, self.height // self.patch, self.width // self.patch)
 
     def with_(self, **kw) -> "EncoderConfig":
         return replace(self, **kw)
@@ -95,4 +97,12 @@ CONFIGS = {
         embed_dim=768, n_layer=12, n_head=12, ffn_dim=3072, n_frames=64, height=384, width=384,
         batch=1, dtype="bf16", rope_layout="interleaved", rope_interpolate=True, seed=4,
         hier_layers=(2, 5, 8, 11), has_mod_embed=True),
+    # Not a configuration of the measured workload: the 2.1 native image path
+    # (one 384 px frame, 576 tokens), the first row after it.
+    "img384": EncoderConfig(
+        name="img384", workload="ViT-B/16 12L 2.1 native image path, bf16, interleaved interpolated RoPE, "
+        "1f 384px (576 tokens), batch 32",
+        embed_dim=768, n_layer=12, n_head=12, ffn_dim=3072, n_frames=1, height=384, width=384,
+        batch=32, dtype="bf16", rope_layout="interleaved", rope_interpolate=True, seed=5,
+        hier_layers=(2, 5, 8, 11), has_mod_embed=True, has_image_path=True),
 }
