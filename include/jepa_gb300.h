@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-#define JEPA_ABI_VERSION 1
+#define JEPA_ABI_VERSION 2  /* 2: jepa_encoder_params.has_image_path */
 
 #if defined(__GNUC__)
 #define JEPA_API __attribute__((visibility("default")))
@@ -67,7 +67,11 @@ typedef enum { JEPA_CLIP_U8_THWC = 0, JEPA_CLIP_F32_CTHW = 1 } jepa_clip_format;
  * dtype: storage type of the 2-D matrices and of the activations fed to the
  * matrix multiplies (F32 = fp32 CUDA-core path; F16/BF16 = tensor-core path
  * with fp32 accumulation).  The residual stream, LayerNorm statistics,
- * softmax and all outputs are fp32 in every mode. */
+ * softmax and all outputs are fp32 in every mode.
+ * has_image_path: the blob also holds the 2.1 native image path (§2
+ * patch_embed_img [D,3,1,16,16] and, with has_mod_embed, img_mod_embed); a
+ * one-frame input then takes it (§3, 2.1 encoder forward; Meta's code selects
+ * it by the frame count). */
 typedef struct jepa_encoder_params {
   int embed_dim, n_layer, n_head, ffn_dim;
   int patch, tubelet;
@@ -77,6 +81,7 @@ typedef struct jepa_encoder_params {
   int hier_layers[4];
   int has_mod_embed;
   int dtype;
+  int has_image_path;
 } jepa_encoder_params;
 
 /* Masked predictor hyper-parameters (same page, §1 "pred.*" rows).
@@ -102,7 +107,9 @@ typedef struct jepa_predictor_params {
  *   attn_qkv.bias [3D], attn_out.weight [D,D], attn_out.bias [D],
  *   ln2.weight, ln2.bias [D], ffn_up.weight [F,D], ffn_up.bias [F],
  *   ffn_down.weight [D,F], ffn_down.bias [D];
- *   norm.weight, norm.bias [D]; then hier_norm.k.weight/bias [D] per tap.
+ *   norm.weight, norm.bias [D]; then hier_norm.k.weight/bias [D] per tap;
+ *   then, if has_image_path: patch_embed_img.weight [D,768] (feature order
+ *   C,H,W), patch_embed_img.bias [D], [mod_embed_img [D] if has_mod_embed].
  * Predictor order: embed.weight [D,in_dim], embed.bias [D], mask_tokens
  *   [n_mask,D] (fp32), the blocks as above, norm.weight/bias, proj.weight
  *   [out_dim,D], proj.bias [out_dim].
@@ -131,8 +138,10 @@ JEPA_API size_t jepa_encode_workspace_bytes(const jepa_encoder* enc, int batch, 
  *         fused form (px - 255*mean)/(255*std) ("Parity ...", Preprocessing
  *         parity); JEPA_CLIP_F32_CTHW: float [batch, 3, n_frames, H, W]
  *         already normalised.
- *   n_frames even, H and W multiples of 16 (non-square allowed), H/16 > 1 and
- *   W/16 > 1 when interpolating RoPE.  N = (n_frames/2)*(H/16)*(W/16).
+ *   n_frames even, or 1 on a model with has_image_path (the 2.1 native image
+ *   path: tubelet 1, patch_embed_img, img_mod_embed, temporal position 0);
+ *   H and W multiples of 16 (non-square allowed), H/16 > 1 and W/16 > 1
+ *   when interpolating RoPE.  N = (n_frames/tubelet)*(H/16)*(W/16).
  *   out_tokens: device float [batch, N, D] = enc.norm(x) (required).
  *   out_pooled: device float [batch, D] token mean of out_tokens, or NULL.
  *   out_hier:   device float [n_hier, batch, N, D] hierarchical taps, or NULL.
@@ -265,6 +274,7 @@ JEPA_API jepa_status jepa_patch_embed_static(const void* clip, const void* weigh
 
 /* Message of the calling thread's last non-OK status ("" if none). */
 JEPA_API const char* jepa_last_error(void);
+/* JEPA_ABI_VERSION of the built library; a binding checks it before use. */
 JEPA_API int jepa_abi_version(void);
 
 #ifdef __cplusplus

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
         assert n in SIGNATURES, f"binding lacks {n}"
-    assert lib.jepa_abi_version() == 1
+    assert lib.jepa_abi_version() == 2
 
 
 def _blob(cfg):
@@ -67,6 +67,24 @@ def test_blob_roundtrip_and_faults(lib):
     with pytest.raises(JepaError) as e:            # bad hierarchical taps
         jg.blob_check(cfg.with_(hier_layers=(1, 1)), blob)
     assert e.value.status == ERR_ARG
+
+
+def test_blob_with_image_path(lib):
+    """The 2.1 image-path tensors follow the hierarchical norms; a blob without
+    them does not satisfy params that ask for them, and the other way round."""
+    import video_vit_encoder_gb300 as jg
+    from video_vit_encoder_gb300._lib import JepaError, ERR_BLOB
+    cfg = synth.CONFIGS["img384"].with_(n_layer=2, hier_layers=(1,))
+    blob = _blob(cfg)
+    jg.blob_check(cfg, blob)
+    assert jg.encoder_tensor_order(cfg)[-3:] == [("patch_embed_img.weight", True), ("patch_embed_img.bias", False),
+                                                 ("mod_embed_img", False)]
+    with pytest.raises(JepaError) as e:
+        jg.blob_check(cfg.with_(has_image_path=False), blob)
+    assert e.value.status == ERR_BLOB
+    with pytest.raises(JepaError) as e:
+        jg.blob_check(cfg, _blob(cfg.with_(has_image_path=False)))
+    assert e.value.status == ERR_BLOB
 
 
 def test_blob_layout_is_aligned(lib):

@@ -30,6 +30,11 @@ SMALL = {
     # V-JEPA 2 geometry, tiled RoPE, head_dim 32, N = 3*5*9 = 135 (ragged against 128-row tiles)
     "v2-hd32": synth.CONFIGS["c3"].with_(embed_dim=256, n_head=8, ffn_dim=512, n_layer=2, n_frames=6,
                                          height=80, width=144, batch=2),
+    # 2.1 native image path (one frame, tubelet 1), N = 6*8 = 48 and 11*5 = 55
+    "img21-bf16": synth.CONFIGS["img384"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=3, height=96,
+                                                width=128, batch=3, hier_layers=(0, 2)),
+    "img21-f16": synth.CONFIGS["img384"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=2, height=176,
+                                               width=80, batch=2, dtype="f16", hier_layers=(1,)),
 }
 
 
@@ -107,4 +112,37 @@ def test_batch_independence(jg):
     one = enc.encode(clip[1:2].contiguous())["out"]
     enc.sync()
     assert_close_16bit(one[0].cpu().numpy(), both[1].cpu().numpy().astype(np.float64), "batch independence")
+    enc.close()
+
+
+def test_one_handle_encodes_clips_and_images(jg):
+    """A model with the image path takes 4-frame clips on the video path and
+    single frames on the image path, from the same handle."""
+    cfg = SMALL["img21-bf16"]
+    w = synth.encoder_weights(cfg)
+    enc = jg.Encoder(cfg, w)
+    for T in (4, 1, 2):
+        c = cfg.with_(n_frames=T)
+        clip = synth.clip_u8(c, batch=2, first_clip=T)
+        got = enc.encode(torch.from_numpy(clip).cuda())["out"].cpu().numpy()
+        enc.sync()
+        for b in range(2):
+            ref = oracle.encoder_forward(c, w, clip[b])
+            assert got.shape[1] == ref["out"].shape[0]
+            assert_close_16bit(got[b], ref["out"], f"T={T} clip {b}")
+    enc.close()
+
+
+@pytest.mark.parametrize("name", ["b21-bf16", "img21-bf16"])
+def test_normalised_float_input(jg, name):
+    """The float [B, 3, T, H, W] input format, already normalised, on the video and image paths."""
+    cfg = SMALL[name]
+    w = synth.encoder_weights(cfg)
+    clip = synth.clip_u8(cfg)
+    xf = np.ascontiguousarray(np.stack([oracle.normalise_clip(clip[b]) for b in range(cfg.batch)]), np.float32)
+    enc = jg.Encoder(cfg, w)
+    got = enc.encode(torch.from_numpy(xf).cuda())["out"].cpu().numpy()
+    enc.sync()
+    for b in range(cfg.batch):
+        assert_close_16bit(got[b], oracle.encoder_forward(cfg, w, clip[b])["out"], f"{name} float input clip {b}")
     enc.close()

@@ -3,6 +3,8 @@
 At these sizes the oracle checks what it can compute in seconds:
   * c3 (ViT-L/16, 8 clips of 16x256x256, the benchmark's launch) - clip 0 end
     to end on every token, clip 7 block by block on sampled rows;
+  * img384 (2.1 native image path, 32 images of 384 px) - two images end to
+    end on every token, with the hierarchical taps;
   * c2, c4, c5 - block by block on sampled rows (each block recomputed by the
     oracle from the GPU's own input residual), the final norm and the
     hierarchical taps on sampled rows, and the c4 predictor end to end.
@@ -155,3 +157,23 @@ def test_c4_encoder_blocks_and_predictor(jg):
     m = assert_close_16bit(out.cpu().numpy(), ref, "c4 predictor")
     print("c4 predictor:", m)
     pred.close()
+
+
+def test_img384_end_to_end(jg):
+    """The 2.1 native image path at its workload size (ViT-B/16, 32 images of
+    384 x 384, 576 tokens each): images 0 and 31 end to end on every token,
+    with the hierarchical taps and the token mean."""
+    cfg = synth.CONFIGS["img384"]
+    w = _weights("img384")
+    clip = synth.clip_u8(cfg)
+    enc = jg.Encoder(cfg, w)
+    res = enc.encode(torch.from_numpy(clip).cuda(), pooled=True, hier=True)
+    enc.sync()
+    for b in (0, cfg.batch - 1):
+        ref = oracle.encoder_forward(cfg, w, clip[b])
+        assert_close_16bit(res["out"][b].cpu().numpy(), ref["out"], f"img384 image {b}")
+        for k, tap in enumerate(ref["hier"]):
+            assert_close_16bit(res["hier"][k, b].cpu().numpy(), tap, f"img384 tap {k} image {b}")
+        np.testing.assert_allclose(res["pooled"][b].cpu().numpy(), ref["pooled"],
+                                   atol=1e-2 * np.abs(ref["pooled"]).max())
+    enc.close()

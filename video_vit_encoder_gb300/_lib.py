@@ -26,11 +26,15 @@ class JepaError(RuntimeError):
         self.status = status
 
 
+ABI_VERSION = 2  # JEPA_ABI_VERSION of include/jepa_gb300.h
+
+
 class EncoderParams(C.Structure):
     _fields_ = [("embed_dim", C.c_int), ("n_layer", C.c_int), ("n_head", C.c_int), ("ffn_dim", C.c_int),
                 ("patch", C.c_int), ("tubelet", C.c_int), ("ln_eps", C.c_float), ("rope_theta", C.c_float),
                 ("rope_layout", C.c_int), ("rope_interpolate", C.c_int), ("rope_ref_grid", C.c_int),
-                ("n_hier", C.c_int), ("hier_layers", C.c_int * 4), ("has_mod_embed", C.c_int), ("dtype", C.c_int)]
+                ("n_hier", C.c_int), ("hier_layers", C.c_int * 4), ("has_mod_embed", C.c_int), ("dtype", C.c_int),
+                ("has_image_path", C.c_int)]
 
 
 class PredictorParams(C.Structure):
@@ -88,6 +92,8 @@ def load(path: str | None = None) -> C.CDLL:
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
+        if lib.jepa_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"{p} has ABI version {lib.jepa_abi_version()}, this binding needs {ABI_VERSION}: rebuild it")
         _lib = lib
         return lib
 

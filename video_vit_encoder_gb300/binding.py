@@ -48,6 +48,10 @@ def encoder_tensor_order(cfg):
     names += [("norm.weight", False), ("norm.bias", False)]
     for k in range(len(cfg.hier_layers)):
         names += [(f"hier_norm.{k}.weight", False), (f"hier_norm.{k}.bias", False)]
+    if getattr(cfg, "has_image_path", False):
+        names += [("patch_embed_img.weight", True), ("patch_embed_img.bias", False)]
+        if cfg.has_mod_embed:
+            names.append(("mod_embed_img", False))
     return names
 
 
@@ -105,6 +109,7 @@ def encoder_params(cfg) -> EncoderParams:
     for i, l in enumerate(cfg.hier_layers):
         p.hier_layers[i] = l
     p.has_mod_embed = int(bool(cfg.has_mod_embed))
+    p.has_image_path = int(bool(getattr(cfg, "has_image_path", False)))
     p.dtype = DTYPE_CODE[cfg.dtype]
     return p
 
@@ -152,7 +157,9 @@ class Encoder:
             pass
 
     def n_tokens(self, T, H, W):
-        return (T // self.cfg.tubelet) * (H // self.cfg.patch) * (W // self.cfg.patch)
+        # one frame on a model with the 2.1 image path: tubelet 1
+        tub = 1 if (T == 1 and getattr(self.cfg, "has_image_path", False)) else self.cfg.tubelet
+        return (T // tub) * (H // self.cfg.patch) * (W // self.cfg.patch)
 
     def encode(self, clip: torch.Tensor, pooled: bool = False, hier: bool = False, out=None, stream=None):
         """clip: uint8 [B,T,H,W,3] (or float [B,3,T,H,W] normalised) on the device."""

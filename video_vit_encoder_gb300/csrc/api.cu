@@ -131,6 +131,11 @@ std::vector<Expect> expected_encoder(const jepa_encoder_params& p) {
     v.push_back({DTYPE_F32, D, 1, 1});
     v.push_back({DTYPE_F32, D, 1, 1});
   }
+  if (p.has_image_path) {  // 2.1 native image path: tubelet-1 patch embedding (+ image modality vector)
+    v.push_back({p.dtype, D, 3u * p.patch * p.patch, 2});
+    v.push_back({DTYPE_F32, D, 1, 1});
+    if (p.has_mod_embed) v.push_back({DTYPE_F32, D, 1, 1});
+  }
   return v;
 }
 
@@ -519,6 +524,8 @@ struct jepa_encoder {
   void* d_weights = nullptr;
   const void* w_pe = nullptr;
   float* b_pe = nullptr;  // patch-embed bias (+ modality vector)
+  const void* w_pe_img = nullptr;  // image path (tubelet 1), when present
+  float* b_pe_img = nullptr;       // its bias (+ image modality vector)
   std::vector<Block> blocks;
   const float *norm_w = nullptr, *norm_b = nullptr;
   const float* hier_w[4] = {};
@@ -540,15 +547,21 @@ namespace {
 
 struct Geom {
   int gt, gh, gw, n_tok;
+  int tub;  // tubelet of this input: 2 for clips, 1 on the image path
 };
 
 jepa_status check_clip(const jepa_encoder* enc, int batch, int T, int H, int W, Geom& g) {
   if (enc == nullptr) return fail(JEPA_ERR_ARG, "encoder handle is NULL");
   if (batch < 1) return fail(JEPA_ERR_ARG, "batch %d must be >= 1", batch);
-  if (T < 2 || T % 2 != 0) return fail(JEPA_ERR_ARG, "n_frames %d must be even and >= 2", T);
+  // One frame takes the 2.1 native image path where the model has it (the
+  // conversion notes, 2.1 encoder forward: selected by the frame count).
+  g.tub = (T == 1 && enc->p.has_image_path) ? 1 : 2;
+  if (g.tub == 2 && (T < 2 || T % 2 != 0))
+    return fail(JEPA_ERR_ARG, "n_frames %d must be even and >= 2%s", T,
+                enc->p.has_image_path ? ", or 1 for an image" : "");
   if (H < 16 || W < 16 || H % 16 != 0 || W % 16 != 0)
     return fail(JEPA_ERR_ARG, "height %d and width %d must be positive multiples of 16", H, W);
-  g.gt = T / 2;
+  g.gt = T / g.tub;
   g.gh = H / 16;
   g.gw = W / 16;
   if (enc->p.rope_interpolate && (g.gh < 2 || g.gw < 2))
@@ -595,14 +608,16 @@ jepa_status embed_into(jepa_encoder* enc, Work& w, const void* clip, int fmt, in
   const int M = batch * g.n_tok;
   Scope sc(enc->prof, P_EMBED, s);
   if (fmt == JEPA_CLIP_U8_THWC)
-    JEPA_TRY(cuda_status(unfold_clip_u8(dt, (const uint8_t*)clip, w.g, batch, T, H, W, s), "unfold"));
+    JEPA_TRY(cuda_status(unfold_clip_u8(dt, (const uint8_t*)clip, w.g, batch, T, H, W, g.tub, s), "unfold"));
   else
-    JEPA_TRY(cuda_status(unfold_clip_f32(dt, (const float*)clip, w.g, batch, T, H, W, s), "unfold"));
+    JEPA_TRY(cuda_status(unfold_clip_f32(dt, (const float*)clip, w.g, batch, T, H, W, g.tub, s), "unfold"));
+  const bool img = g.tub == 1;
   EpiParams ep{};
-  ep.bias = enc->b_pe;
+  ep.bias = img ? enc->b_pe_img : enc->b_pe;
   ep.out = x_out;
   ep.ldo = D;
-  return run_linear(dt, EPI_F32, w.g, enc->w_pe, M, D, 1536, ep, enc->d_status, s, enc->sms);
+  return run_linear(dt, EPI_F32, w.g, img ? enc->w_pe_img : enc->w_pe, M, D, 768 * g.tub, ep, enc->d_status, s,
+                    enc->sms);
 }
 
 }  // namespace
@@ -661,6 +676,17 @@ jepa_status jepa_encoder_create(const void* blob, size_t blob_bytes, const jepa_
     enc->hier_w[k] = (const float*)P[i++];
     enc->hier_b[k] = (const float*)P[i++];
   }
+  if (params->has_image_path) {
+    enc->w_pe_img = P[i++];
+    const float* b_img = (const float*)P[i++];
+    const float* mod_img = params->has_mod_embed ? (const float*)P[i++] : nullptr;
+    if (cudaMalloc(&enc->b_pe_img, D * sizeof(float)) != cudaSuccess) {
+      jepa_encoder_destroy(enc);
+      return fail(JEPA_ERR_OOM, "encoder: small allocations failed");
+    }
+    cudaMemcpy(enc->b_pe_img, b_img, D * sizeof(float), cudaMemcpyDeviceToDevice);
+    if (mod_img) add_vec_kernel<<<(D + 255) / 256, 256>>>(enc->b_pe_img, mod_img, D);
+  }
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     jepa_encoder_destroy(enc);
@@ -676,6 +702,7 @@ void jepa_encoder_destroy(jepa_encoder* enc) {
   cudaDeviceSynchronize();
   cudaFree(enc->d_weights);
   cudaFree(enc->b_pe);
+  cudaFree(enc->b_pe_img);
   cudaFree(enc->ws);
   cudaFree(enc->d_status);
   cudaFree(enc->rope.d);

@@ -33,9 +33,10 @@ cudaError_t attention_simt(int dtype, const void* q, const void* k, const void* 
                            int n_tok, int head_dim, int ldv, float scale, cudaStream_t s);
 
 // Element-wise / row-wise kernels.
-cudaError_t unfold_clip_u8(int dtype, const uint8_t* clip, void* out, int batch, int T, int H, int W,
+// tubelet 2 (clips) or 1 (the 2.1 image path): rows of 3 * tubelet * 256.
+cudaError_t unfold_clip_u8(int dtype, const uint8_t* clip, void* out, int batch, int T, int H, int W, int tubelet,
                            cudaStream_t s);
-cudaError_t unfold_clip_f32(int dtype, const float* clip, void* out, int batch, int T, int H, int W,
+cudaError_t unfold_clip_f32(int dtype, const float* clip, void* out, int batch, int T, int H, int W, int tubelet,
                             cudaStream_t s);
 cudaError_t layernorm(int out_dtype, const float* x, const float* w, const float* b, void* y, int rows, int dim,
                       float eps, cudaStream_t s);

@@ -106,7 +106,7 @@ extern "C" jepa_status jepa_patch_embed_static(const void* clip, const void* wei
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The unfold overwrites every scratch row the GEMM then reads, so nothing
   // needs clearing between calls.
-  if (unfold_clip_u8(dtype, static_cast<const uint8_t*>(clip), scratch, batch, n_frames, height, width, s) !=
+  if (unfold_clip_u8(dtype, static_cast<const uint8_t*>(clip), scratch, batch, n_frames, height, width, 2, s) !=
       cudaSuccess)
     return err(JEPA_ERR_CUDA, "jepa_patch_embed_static: unfold launch failed");
   EpiParams ep{};

@@ -15,38 +15,40 @@ __constant__ float c_std255[3] = {255.0f * 0.229f, 255.0f * 0.224f, 255.0f * 0.2
 
 // One thread per (token, dt, y): reads the 16 pixels x 3 channels of one
 // tubelet row (48 contiguous bytes of the THWC clip) and writes the three
-// 16-wide runs c*512 + dt*256 + y*16 + [0,16) of the token's 1536-wide row
-// (the row-major C,T,H,W flattening of the Conv3d kernel, conversion notes §2).
-template <typename T>
+// 16-wide runs c*(TUB*256) + dt*256 + y*16 + [0,16) of the token's
+// 3*TUB*256-wide row (the row-major C,T,H,W flattening of the Conv3d kernel,
+// conversion notes §2).  TUB = 2 for clips, 1 for the 2.1 image path.
+template <typename T, int TUB>
 __global__ void unfold_u8_kernel(const uint8_t* __restrict__ clip, T* __restrict__ out, int batch, int T_, int H,
                                  int W) {
-  const int gt = T_ >> 1, gh = H >> 4, gw = W >> 4;
+  constexpr int K = 3 * TUB * 256;
+  const int gt = T_ / TUB, gh = H >> 4, gw = W >> 4;
   const long n_tok = (long)gt * gh * gw;
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long total = (long)batch * n_tok * 32;
+  const long total = (long)batch * n_tok * 16 * TUB;
   if (idx >= total) return;
   const int y = idx & 15;
-  const int dt = (idx >> 4) & 1;
-  const long row = idx >> 5;
+  const int dt = (int)((idx >> 4) % TUB);
+  const long row = (idx >> 4) / TUB;
   const long b = row / n_tok;
   const long tok = row - b * n_tok;
   const int t = tok / (gh * gw);
   const int rem = tok - (long)t * gh * gw;
   const int hh = rem / gw, ww = rem - hh * gw;
-  const long frame = (long)b * T_ + 2 * t + dt;
+  const long frame = (long)b * T_ + TUB * t + dt;
   const uint8_t* src = clip + ((frame * H + 16 * hh + y) * (long)W + 16 * ww) * 3;
   uint4 raw[3];
   raw[0] = __ldg(reinterpret_cast<const uint4*>(src));
   raw[1] = __ldg(reinterpret_cast<const uint4*>(src) + 1);
   raw[2] = __ldg(reinterpret_cast<const uint4*>(src) + 2);
   const uint8_t* px = reinterpret_cast<const uint8_t*>(raw);
-  T* dst = out + row * 1536 + dt * 256 + y * 16;
+  T* dst = out + row * K + dt * 256 + y * 16;
 #pragma unroll
   for (int c = 0; c < 3; ++c) {
     float v[16];
 #pragma unroll
     for (int x = 0; x < 16; ++x) v[x] = ((float)px[3 * x + c] - c_mean255[c]) / c_std255[c];
-    T* d = dst + c * 512;
+    T* d = dst + c * (TUB * 256);
     if constexpr (sizeof(T) == 2) {
       uint4 u0, u1;
       u0.x = pack2<T>(v[0], v[1]);   u0.y = pack2<T>(v[2], v[3]);
@@ -65,17 +67,18 @@ __global__ void unfold_u8_kernel(const uint8_t* __restrict__ clip, T* __restrict
 
 // Same unfold from an already normalised float clip [batch, 3, T, H, W]:
 // one thread per (token, c, dt, y) copies 16 floats.
-template <typename T>
+template <typename T, int TUB>
 __global__ void unfold_f32_kernel(const float* __restrict__ clip, T* __restrict__ out, int batch, int T_, int H,
                                   int W) {
-  const int gt = T_ >> 1, gh = H >> 4, gw = W >> 4;
+  constexpr int K = 3 * TUB * 256;
+  const int gt = T_ / TUB, gh = H >> 4, gw = W >> 4;
   const long n_tok = (long)gt * gh * gw;
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long total = (long)batch * n_tok * 96;
+  const long total = (long)batch * n_tok * 48 * TUB;
   if (idx >= total) return;
   const int y = idx & 15;
-  const int dt = (idx >> 4) & 1;
-  const long r2 = idx >> 5;
+  const int dt = (int)((idx >> 4) % TUB);
+  const long r2 = (idx >> 4) / TUB;
   const int c = r2 % 3;
   const long row = r2 / 3;
   const long b = row / n_tok;
@@ -83,11 +86,11 @@ __global__ void unfold_f32_kernel(const float* __restrict__ clip, T* __restrict_
   const int t = tok / (gh * gw);
   const int rem = tok - (long)t * gh * gw;
   const int hh = rem / gw, ww = rem - hh * gw;
-  const float* src = clip + ((((b * 3 + c) * T_ + 2 * t + dt) * (long)H + 16 * hh + y) * W + 16 * ww);
+  const float* src = clip + ((((b * 3 + c) * T_ + TUB * t + dt) * (long)H + 16 * hh + y) * W + 16 * ww);
   float v[16];
 #pragma unroll
   for (int x = 0; x < 16; ++x) v[x] = __ldg(src + x);
-  T* d = out + row * 1536 + c * 512 + dt * 256 + y * 16;
+  T* d = out + row * K + c * (TUB * 256) + dt * 256 + y * 16;
 #pragma unroll
   for (int x = 0; x < 16; ++x) d[x] = DT<T>::from(v[x]);
 }
@@ -239,28 +242,40 @@ inline unsigned grid_for(long n, int block) { return (unsigned)((n + block - 1) 
 
 }  // namespace
 
-cudaError_t unfold_clip_u8(int dtype, const uint8_t* clip, void* out, int batch, int T, int H, int W,
-                           cudaStream_t s) {
-  const long total = (long)batch * (T / 2) * (H / 16) * (W / 16) * 32;
+template <int TUB>
+cudaError_t unfold_u8_t(int dtype, const uint8_t* clip, void* out, int batch, int T, int H, int W, cudaStream_t s) {
+  const long total = (long)batch * (T / TUB) * (H / 16) * (W / 16) * 16 * TUB;
   if (dtype == DTYPE_BF16)
-    unfold_u8_kernel<__nv_bfloat16><<<grid_for(total, 256), 256, 0, s>>>(clip, (__nv_bfloat16*)out, batch, T, H, W);
+    unfold_u8_kernel<__nv_bfloat16, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__nv_bfloat16*)out, batch, T, H, W);
   else if (dtype == DTYPE_F16)
-    unfold_u8_kernel<__half><<<grid_for(total, 256), 256, 0, s>>>(clip, (__half*)out, batch, T, H, W);
+    unfold_u8_kernel<__half, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__half*)out, batch, T, H, W);
   else
-    unfold_u8_kernel<float><<<grid_for(total, 256), 256, 0, s>>>(clip, (float*)out, batch, T, H, W);
+    unfold_u8_kernel<float, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (float*)out, batch, T, H, W);
   return cudaGetLastError();
 }
 
-cudaError_t unfold_clip_f32(int dtype, const float* clip, void* out, int batch, int T, int H, int W,
-                            cudaStream_t s) {
-  const long total = (long)batch * (T / 2) * (H / 16) * (W / 16) * 96;
+template <int TUB>
+cudaError_t unfold_f32_t(int dtype, const float* clip, void* out, int batch, int T, int H, int W, cudaStream_t s) {
+  const long total = (long)batch * (T / TUB) * (H / 16) * (W / 16) * 48 * TUB;
   if (dtype == DTYPE_BF16)
-    unfold_f32_kernel<__nv_bfloat16><<<grid_for(total, 256), 256, 0, s>>>(clip, (__nv_bfloat16*)out, batch, T, H, W);
+    unfold_f32_kernel<__nv_bfloat16, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__nv_bfloat16*)out, batch, T, H, W);
   else if (dtype == DTYPE_F16)
-    unfold_f32_kernel<__half><<<grid_for(total, 256), 256, 0, s>>>(clip, (__half*)out, batch, T, H, W);
+    unfold_f32_kernel<__half, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__half*)out, batch, T, H, W);
   else
-    unfold_f32_kernel<float><<<grid_for(total, 256), 256, 0, s>>>(clip, (float*)out, batch, T, H, W);
+    unfold_f32_kernel<float, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (float*)out, batch, T, H, W);
   return cudaGetLastError();
+}
+
+cudaError_t unfold_clip_u8(int dtype, const uint8_t* clip, void* out, int batch, int T, int H, int W, int tubelet,
+                           cudaStream_t s) {
+  return tubelet == 1 ? unfold_u8_t<1>(dtype, clip, out, batch, T, H, W, s)
+                      : unfold_u8_t<2>(dtype, clip, out, batch, T, H, W, s);
+}
+
+cudaError_t unfold_clip_f32(int dtype, const float* clip, void* out, int batch, int T, int H, int W, int tubelet,
+                            cudaStream_t s) {
+  return tubelet == 1 ? unfold_f32_t<1>(dtype, clip, out, batch, T, H, W, s)
+                      : unfold_f32_t<2>(dtype, clip, out, batch, T, H, W, s);
 }
 
 cudaError_t layernorm(int out_dtype, const float* x, const float* w, const float* b, void* y, int rows, int dim,
