@@ -11,6 +11,11 @@ LayerNorm), inputs already resident in HBM.  The L2 cache (129 MB) is flushed
 between timed steps by writing a 256 MB buffer outside the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload vitl16-16f256 | vitb16-img384]
+
+--workload vitb16-img384 measures the V-JEPA 2.1 native image path instead
+(ViT-B/16, 32 images of 384 x 384, 576 tokens each) and prints the same line
+for that workload.
 
 Under torchrun (N > 1) every rank runs its own replica (weak scaling, no
 collective on the data path); rank 0 prints one JSON line.
@@ -30,9 +35,18 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "encoder tokens/sec (ViT-L/16, 16f 256px, bf16) and % of bf16 tensor peak"
 UNIT = "tokens/s"
-WORKLOAD = "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 16f x 256x256 (2048 tokens/clip), batch 8 per GPU"
+# name -> (seeded config, metric, workload description)
+WORKLOADS = {
+    "vitl16-16f256": ("c3", "encoder tokens/sec (ViT-L/16, 16f 256px, bf16) and % of bf16 tensor peak",
+                      "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 16f x 256x256 (2048 tokens/clip), "
+                      "batch 8 per GPU"),
+    "vitb16-img384": ("img384", "encoder tokens/sec (V-JEPA 2.1 ViT-B/16 native image path, 384px, bf16) and % of "
+                      "bf16 tensor peak",
+                      "ViT-B/16 12L D768 h12 FFN3072, bf16, 2.1 native image path (tubelet 1, patch_embed_img), "
+                      "interleaved interpolated RoPE, 1f x 384x384 (576 tokens/image), batch 32 per GPU"),
+}
+DEFAULT_WORKLOAD = "vitl16-16f256"
 CLASSES = ["patch_embed", "layernorm", "qkv_gemm", "attention", "out_proj_gemm", "ffn_up_gemm", "ffn_down_gemm",
            "other"]
 
@@ -47,17 +61,23 @@ def _peaks():
     return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def _patch_k(cfg):
+    """Width of one token's unfolded pixels: 3 x tubelet x 16 x 16 (tubelet 1 on the image path)."""
+    tub = 1 if (cfg.n_frames == 1 and cfg.has_image_path) else cfg.tubelet
+    return 3 * tub * cfg.patch * cfg.patch
+
+
 def flops_per_clip(cfg, n_tok):
-    """Algorithmic FLOPs of one clip: per token L*(24 D^2 + 4 N D) + 2*1536*D."""
+    """Algorithmic FLOPs of one clip: per token L*(24 D^2 + 4 N D) + 2*K_patch*D."""
     D, L, F = cfg.embed_dim, cfg.n_layer, cfg.ffn_dim
     per_tok_layer = 2 * (3 * D * D + D * D + 2 * D * F) + 4 * n_tok * D
-    return n_tok * (L * per_tok_layer + 2 * 1536 * D)
+    return n_tok * (L * per_tok_layer + 2 * _patch_k(cfg) * D)
 
 
 def class_flops_per_launch(cfg, batch, n_tok):
     D, F, H = cfg.embed_dim, cfg.ffn_dim, cfg.n_head
     M = batch * n_tok
-    return {"patch_embed": 2 * M * 1536 * D, "qkv_gemm": 2 * M * D * 3 * D, "attention": 4 * batch * H * n_tok * n_tok * (D // H),
+    return {"patch_embed": 2 * M * _patch_k(cfg) * D, "qkv_gemm": 2 * M * D * 3 * D, "attention": 4 * batch * H * n_tok * n_tok * (D // H),
             "out_proj_gemm": 2 * M * D * D, "ffn_up_gemm": 2 * M * D * F, "ffn_down_gemm": 2 * M * F * D}
 
 
@@ -189,7 +209,8 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    cfg = synth.CONFIGS["c3"]
+    key, metric, workload = WORKLOADS[args.workload]
+    cfg = synth.CONFIGS[key]
     w = synth.encoder_weights(cfg)
     clip = synth.clip_u8(cfg, batch=1)[0]
     vals = []
@@ -199,10 +220,11 @@ def run_reference(args):
             vals.append(r)
     v = statistics.median(x["value"] for x in vals)
     sec = statistics.median(x["seconds_per_clip"] for x in vals)
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1000.0 * cfg.batch,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": cfg.batch, "seq_len": 2048, "parallelism": "none",
+            "config": {"workload": workload, "global_batch": cfg.batch, "seq_len": synth.tokens_per_clip(cfg),
+                       "parallelism": "none",
                        "note": "CPU oracle; one clip sampled per step, scaled to the batch"},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": vals[0]["cores"], "kind": "oracle",
                              "sample": vals[0]["sample"].replace(" + 1 of", " + 1 of")},
@@ -219,6 +241,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -240,7 +263,8 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    cfg = synth.CONFIGS["c3"]
+    key, metric, workload = WORKLOADS[args.workload]
+    cfg = synth.CONFIGS[key]
     B = cfg.batch
     n_tok = synth.tokens_per_clip(cfg)
     weights = synth.encoder_weights(cfg)
@@ -310,10 +334,10 @@ def main():
     e2e_val = world * B * n_tok / e2e_s
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) weights, uniform uint8 clips)",
-        "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": n_tok,
+        "config": {"workload": workload, "global_batch": B * world, "seq_len": n_tok,
                    "parallelism": f"replicas x{world}" if world > 1 else "none",
                    "l2": "flushed between timed steps (256 MB write outside the timed region)"},
         "clips_per_s": value / n_tok,
@@ -325,9 +349,11 @@ def main():
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(hclip.numel()),
                 "d2h_bytes_per_step": int(hout.numel() * 4), "api": "jepa_encode_host (pinned host buffers)"},
         "clocks": clocks.summary(),
-        "context_baseline": {"value": 2048 / 0.0465, "unit": UNIT,
-                             "what": "pages' ggml-CUDA f16 ViT-L/16 16f 256px, batch 1, RTX 4500 Ada (context only)"},
     }
+    if args.workload == DEFAULT_WORKLOAD:
+        line["context_baseline"] = {"value": 2048 / 0.0465, "unit": UNIT,
+                                    "what": "pages' ggml-CUDA f16 ViT-L/16 16f 256px, batch 1, RTX 4500 Ada "
+                                            "(context only)"}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, weights, clip_np[0], blocks=4)
         line["cpu_baseline"].pop("seconds_per_clip", None)
