@@ -315,31 +315,47 @@ def encoder_forward(cfg, wts, clip_u8, n_layers: int | None = None, return_resid
 
 
 # ----------------------------------------------------------------------------- predictor
-def predictor_input(pcfg, pwts, enc_out, ids_ctx, ids_tgt):
-    """Predictor token sequence before its blocks ([N] §3 predictor forward, §4.4).
+def predictor_input(pcfg, pwts, enc_out, ids_ctx, ids_tgt, modality: str = "video"):
+    """Predictor token sequence before its blocks ([N] §3 predictor forwards, §4.4).
 
     ctx = enc_out[ids_ctx] W_emb^T + b_emb; every target row is the mask token
     ``mask_tokens[mask_index % n_mask_tokens]``; the sequence is ctx then tgt.
+    The 2.1 predictor then adds its own modality vector (``mod_embed_video``,
+    or ``mod_embed_img`` for the image path) to every row.
     """
     ctx = _linear(np.asarray(enc_out, F64)[np.asarray(ids_ctx)], pwts["embed.weight"], pwts["embed.bias"])
     m = np.asarray(pwts["mask_tokens"], F64)[pcfg.mask_index % pcfg.n_mask_tokens]
     tgt = np.broadcast_to(m, (len(ids_tgt), m.shape[0]))
-    return np.concatenate([ctx, tgt], axis=0)
+    z = np.concatenate([ctx, tgt], axis=0)
+    if getattr(pcfg, "has_mod_embed", False):
+        z = z + np.asarray(pwts[f"mod_embed_{'img' if modality == 'image' else 'video'}"], F64)
+    return z
 
 
-def predictor_forward(pcfg, pwts, enc_out, ids_ctx, ids_tgt, grid):
-    """V-JEPA 2 masked predictor ([N] §2 key map, §3 predictor forward, §4.4).
+def predictor_outputs(pcfg, pwts, enc_out, ids_ctx, ids_tgt, grid, modality: str = "video"):
+    """Masked predictor ([N] §2 key maps, §3 predictor forwards, §4.4).
 
-    Blocks as the encoder's (head_dim 32, tiled RoPE from the ids on the full
-    encoder grid, no interpolation), then pred.norm, then pred.proj on the
-    target rows.  Context and target rows with the same id share a position.
+    Blocks as the encoder's (head_dim 32, RoPE from the ids on the full
+    encoder grid, no interpolation; tiled for V-JEPA 2, interleaved for 2.1),
+    then pred.norm.  ``pred`` = pred.proj on the target rows; ``ctx`` =
+    pred.proj_context on the context rows where the model has it (2.1), else
+    None.  Context and target rows with the same id share a position.
     """
     gt, gh, gw = grid
-    z = predictor_input(pcfg, pwts, enc_out, ids_ctx, ids_tgt)
+    z = predictor_input(pcfg, pwts, enc_out, ids_ctx, ids_tgt, modality)
     ids = np.concatenate([np.asarray(ids_ctx), np.asarray(ids_tgt)])
     pos = grid_positions_from_ids(ids, gt, gh, gw)
     COS, SIN = rope_tables(pos, pcfg.embed_dim // pcfg.n_head, pcfg.rope_layout, pcfg.rope_theta)
     for i in range(pcfg.n_layer):
         z = block_forward(z, pwts, i, pcfg.n_head, pcfg.ln_eps, COS, SIN)
     z = layer_norm(z, pwts["norm.weight"], pwts["norm.bias"], pcfg.ln_eps)
-    return _linear(z[len(ids_ctx):], pwts["proj.weight"], pwts["proj.bias"])
+    n_ctx = len(ids_ctx)
+    out = {"pred": _linear(z[n_ctx:], pwts["proj.weight"], pwts["proj.bias"]), "ctx": None}
+    if getattr(pcfg, "has_proj_context", False):
+        out["ctx"] = _linear(z[:n_ctx], pwts["proj_context.weight"], pwts["proj_context.bias"])
+    return out
+
+
+def predictor_forward(pcfg, pwts, enc_out, ids_ctx, ids_tgt, grid, modality: str = "video"):
+    """The target predictions of :func:`predictor_outputs`."""
+    return predictor_outputs(pcfg, pwts, enc_out, ids_ctx, ids_tgt, grid, modality)["pred"]

@@ -21,10 +21,10 @@ from __future__ import annotations
 
 import numpy as np
 
-from .configs import CONFIGS, EncoderConfig, PredictorConfig, tokens_per_clip
+from .configs import CONFIGS, PREDICTOR_21, EncoderConfig, PredictorConfig, tokens_per_clip
 
 __all__ = [
-    "GOLDEN", "CONFIGS", "EncoderConfig", "PredictorConfig", "tokens_per_clip",
+    "GOLDEN", "CONFIGS", "PREDICTOR_21", "EncoderConfig", "PredictorConfig", "tokens_per_clip",
     "mix64", "draws_u64", "uniform_u8", "normal", "round_to_dtype",
     "bf16_bits", "f16_bits", "bits_to_f32",
     "encoder_weights", "predictor_weights", "clip_u8", "context_target_split",
@@ -179,6 +179,11 @@ def tensor_names_predictor(pc: PredictorConfig):
         ]
     out += [("norm.weight", (D,), "one"), ("norm.bias", (D,), "zero"),
             ("proj.weight", (pc.out_dim, D), "mat"), ("proj.bias", (pc.out_dim,), "zero")]
+    # 2.1 additions, appended last so no other tensor's stream moves
+    if pc.has_mod_embed:
+        out += [("mod_embed_video", (D,), "vec"), ("mod_embed_img", (D,), "vec")]
+    if pc.has_proj_context:
+        out += [("proj_context.weight", (pc.out_dim, D), "mat"), ("proj_context.bias", (pc.out_dim,), "zero")]
     return out
 
 

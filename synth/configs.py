@@ -28,6 +28,13 @@ class PredictorConfig:
     ln_eps: float = 1e-6
     rope_theta: float = 10000.0
     rope_layout: str = "tiled"
+    has_mod_embed: bool = False     # 2.1: pred.mod_embed_video / pred.mod_embed_img on every row
+    has_proj_context: bool = False  # 2.1: pred.proj_context on the context rows
+
+
+# The V-JEPA 2.1 ViT-B/16 384 predictor (conversion notes §1 "pred.*" rows).
+PREDICTOR_21 = PredictorConfig(in_dim=768, out_dim=1664, n_mask_tokens=8, rope_layout="interleaved",
+                               has_mod_embed=True, has_proj_context=True)
 
 
 @dataclass(frozen=True)
@@ -105,4 +112,13 @@ CONFIGS = {
         embed_dim=768, n_layer=12, n_head=12, ffn_dim=3072, n_frames=1, height=384, width=384,
         batch=32, dtype="bf16", rope_layout="interleaved", rope_interpolate=True, seed=5,
         hier_layers=(2, 5, 8, 11), has_mod_embed=True, has_image_path=True),
+    # Not a configuration of the measured workload: the 2.1 predictor on the
+    # 2.1 ViT-B/16 16f 384 px clip (4608 tokens, grid 8 x 24 x 24), the second
+    # row after it.
+    "pred21": EncoderConfig(
+        name="pred21", workload="ViT-B/16 12L 2.1 encoder + 2.1 masked predictor (D384 L12 hd32, 8 mask tokens, "
+        "out 1664, context projection), bf16, 16f 384px (4608 tokens), batch 1",
+        embed_dim=768, n_layer=12, n_head=12, ffn_dim=3072, n_frames=16, height=384, width=384,
+        batch=1, dtype="bf16", rope_layout="interleaved", rope_interpolate=True, seed=6,
+        hier_layers=(2, 5, 8, 11), has_mod_embed=True, has_image_path=True, predictor=PREDICTOR_21),
 }

@@ -5,6 +5,8 @@ linear, scaled_dot_product_attention, erf GELU) with the RoPE tables of the
 conversion notes §4 must reproduce the oracle; structural cases (zeroed
 blocks, row sampling, permutations) pin the rest.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -154,11 +156,13 @@ def _pred_setup(seed=0):
     return cfg, pw, enc, ctx, tgt, (gt, gh, gw)
 
 
-def _torch_predictor(pc, pw, enc, ctx, tgt, grid):
+def _torch_predictor(pc, pw, enc, ctx, tgt, grid, modality="video", with_ctx=False):
     D = pc.embed_dim
     z_ctx = Fn.linear(_t(enc)[torch.from_numpy(ctx).long()], _t(pw["embed.weight"]), _t(pw["embed.bias"]))
     m = _t(pw["mask_tokens"])[pc.mask_index % pc.n_mask_tokens]
     z = torch.cat([z_ctx, m.expand(len(tgt), D)], 0)
+    if pc.has_mod_embed:
+        z = z + _t(pw["mod_embed_img" if modality == "image" else "mod_embed_video"])
     ids = torch.from_numpy(np.concatenate([ctx, tgt])).long()
     gt, gh, gw = grid
     pos = torch.stack([ids // (gh * gw), (ids % (gh * gw)) // gw, ids % gw], 1).double()
@@ -175,7 +179,10 @@ def _torch_predictor(pc, pw, enc, ctx, tgt, grid):
         z = z + Fn.linear(Fn.gelu(Fn.linear(y, _t(pw[p + "ffn_up.weight"]), _t(pw[p + "ffn_up.bias"]))),
                           _t(pw[p + "ffn_down.weight"]), _t(pw[p + "ffn_down.bias"]))
     z = Fn.layer_norm(z, (D,), _t(pw["norm.weight"]), _t(pw["norm.bias"]), pc.ln_eps)
-    return Fn.linear(z[len(ctx):], _t(pw["proj.weight"]), _t(pw["proj.bias"])).numpy()
+    pred = Fn.linear(z[len(ctx):], _t(pw["proj.weight"]), _t(pw["proj.bias"])).numpy()
+    if not with_ctx:
+        return pred
+    return pred, Fn.linear(z[:len(ctx)], _t(pw["proj_context.weight"]), _t(pw["proj_context.bias"])).numpy()
 
 
 def test_predictor_matches_torch_composition():
@@ -204,3 +211,82 @@ def test_predictor_target_permutation_equivariant():
     perm = np.random.default_rng(0).permutation(len(tgt))
     b = oracle.predictor_forward(cfg.predictor, pw, enc, ctx, tgt[perm], grid)
     np.testing.assert_allclose(a[perm], b, atol=1e-11)
+
+
+# ----------------------------------------------------------------------------- 2.1 predictor
+# [conversion notes §3, 2.1 predictor forward]: the modality vector on every
+# row, interleaved RoPE from the ids on the fixed 24-grid with no
+# interpolation, pred.norm, pred.proj on the target rows and
+# pred.proj_context on the context rows.
+PRED21_CFG = synth.CONFIGS["pred21"].with_(
+    n_frames=4, height=96, width=96,
+    predictor=dataclasses.replace(synth.PREDICTOR_21, n_layer=2))
+
+
+def _pred21_setup(seed=0, image=False):
+    cfg = PRED21_CFG.with_(n_frames=1) if image else PRED21_CFG
+    pw = _perturb_lns(synth.predictor_weights(cfg), seed)
+    rng = np.random.default_rng(seed)
+    for k in ("mod_embed_video", "mod_embed_img"):
+        pw[k] = rng.standard_normal(pw[k].shape) * 0.5        # visible against the 0.02-scale weights
+    gt, gh, gw = cfg.grid()
+    n = gt * gh * gw
+    enc = rng.standard_normal((n, 768))
+    ctx, tgt = synth.context_target_split(cfg)
+    return cfg, pw, enc, ctx, tgt, (gt, gh, gw)
+
+
+@pytest.mark.parametrize("image", [False, True])
+def test_predictor21_matches_torch_composition(image):
+    cfg, pw, enc, ctx, tgt, grid = _pred21_setup(3, image)
+    mod = "image" if image else "video"
+    got = oracle.predictor_outputs(cfg.predictor, pw, enc, ctx, tgt, grid, mod)
+    assert got["pred"].shape == (len(tgt), 1664) and got["ctx"].shape == (len(ctx), 1664)
+    ref_pred, ref_ctx = _torch_predictor(cfg.predictor, pw, enc, ctx, tgt, grid, mod, with_ctx=True)
+    np.testing.assert_allclose(got["pred"], ref_pred, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(got["ctx"], ref_ctx, rtol=0, atol=1e-10)
+
+
+def test_predictor21_zero_blocks_closed_form():
+    """With every block zeroed the blocks are the identity, so each target row
+    is proj(norm(mask token + modality vector)) and each context row
+    proj_context(norm(embed(enc row) + modality vector))."""
+    cfg, pw, enc, ctx, tgt, grid = _pred21_setup(4)
+    pc = cfg.predictor
+    for k in list(pw):
+        if k.startswith("blk."):
+            pw[k] = np.zeros_like(pw[k])
+    got = oracle.predictor_outputs(pc, pw, enc, ctx, tgt, grid, "video")
+    mod = pw["mod_embed_video"].astype(np.float64)
+    m = pw["mask_tokens"][pc.mask_index % pc.n_mask_tokens].astype(np.float64) + mod
+    zt = oracle.layer_norm(m[None], pw["norm.weight"], pw["norm.bias"], pc.ln_eps)
+    exp_t = zt @ pw["proj.weight"].astype(np.float64).T + pw["proj.bias"]
+    np.testing.assert_allclose(got["pred"], np.broadcast_to(exp_t, got["pred"].shape), rtol=0, atol=1e-12)
+    e = enc[ctx] @ pw["embed.weight"].astype(np.float64).T + pw["embed.bias"] + mod
+    zc = oracle.layer_norm(e, pw["norm.weight"], pw["norm.bias"], pc.ln_eps)
+    exp_c = zc @ pw["proj_context.weight"].astype(np.float64).T + pw["proj_context.bias"]
+    np.testing.assert_allclose(got["ctx"], exp_c, rtol=0, atol=1e-12)
+
+
+def test_predictor21_context_permutation_equivariant():
+    """Permuting the context ids permutes the context outputs and leaves the
+    target predictions unchanged (attention with positions attached is
+    permutation-equivariant)."""
+    cfg, pw, enc, ctx, tgt, grid = _pred21_setup(5)
+    a = oracle.predictor_outputs(cfg.predictor, pw, enc, ctx, tgt, grid)
+    perm = np.random.default_rng(1).permutation(len(ctx))
+    b = oracle.predictor_outputs(cfg.predictor, pw, enc, ctx[perm], tgt, grid)
+    np.testing.assert_allclose(b["ctx"], a["ctx"][perm], atol=1e-11)
+    np.testing.assert_allclose(b["pred"], a["pred"], atol=1e-11)
+
+
+def test_predictor21_mask_token_and_modality():
+    cfg, pw, enc, ctx, tgt, grid = _pred21_setup(6)
+    pc = cfg.predictor
+    assert pc.n_mask_tokens == 8 and pc.mask_index % pc.n_mask_tokens == 1
+    z = oracle.predictor_input(pc, pw, enc, ctx, tgt, "image")
+    exp = pw["mask_tokens"][1].astype(np.float64) + pw["mod_embed_img"]
+    np.testing.assert_array_equal(z[len(ctx):], np.broadcast_to(exp, (len(tgt), 384)))
+    zv = oracle.predictor_input(pc, pw, enc, ctx, tgt, "video")
+    np.testing.assert_allclose(z - zv, np.broadcast_to(pw["mod_embed_img"] - pw["mod_embed_video"], z.shape),
+                               atol=1e-12)
