@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-#define JEPA_ABI_VERSION 2  /* 2: jepa_encoder_params.has_image_path */
+#define JEPA_ABI_VERSION 3  /* 2: jepa_encoder_params.has_image_path; 3: 2.1 predictor fields */
 
 #if defined(__GNUC__)
 #define JEPA_API __attribute__((visibility("default")))
@@ -56,6 +56,9 @@ typedef enum {
 typedef enum { JEPA_DT_F32 = 0, JEPA_DT_F16 = 1, JEPA_DT_BF16 = 2 } jepa_dtype;
 typedef enum { JEPA_ROPE_TILED = 0, JEPA_ROPE_INTERLEAVED = 1 } jepa_rope_layout;
 typedef enum { JEPA_CLIP_U8_THWC = 0, JEPA_CLIP_F32_CTHW = 1 } jepa_clip_format;
+/* Which 2.1 predictor modality vector joins every row (AUTO: image for a
+ * grid of one temporal slice, the grid of the 2.1 image path). */
+typedef enum { JEPA_MODALITY_VIDEO = 0, JEPA_MODALITY_IMAGE = 1, JEPA_MODALITY_AUTO = 2 } jepa_modality;
 
 /* Encoder hyper-parameters ("V-JEPA 2 / 2.1 tensor maps and RoPE derivation",
  * §1).  head_dim = embed_dim / n_head must be 32 or 64.  patch must be 16 and
@@ -93,6 +96,8 @@ typedef struct jepa_predictor_params {
   float ln_eps, rope_theta;
   int rope_layout;
   int dtype;
+  int has_mod_embed;     /* 2.1: pred.mod_embed_video / pred.mod_embed_img added to every row (§3) */
+  int has_proj_context;  /* 2.1: pred.proj_context [out_dim,D] on the context rows (§2, §3) */
 } jepa_predictor_params;
 
 /* ---------------------------------------------------------------- weight blob
@@ -112,7 +117,9 @@ typedef struct jepa_predictor_params {
  *   C,H,W), patch_embed_img.bias [D], [mod_embed_img [D] if has_mod_embed].
  * Predictor order: embed.weight [D,in_dim], embed.bias [D], mask_tokens
  *   [n_mask,D] (fp32), the blocks as above, norm.weight/bias, proj.weight
- *   [out_dim,D], proj.bias [out_dim].
+ *   [out_dim,D], proj.bias [out_dim]; then [mod_embed_video [D],
+ *   mod_embed_img [D] if has_mod_embed]; then [proj_context.weight
+ *   [out_dim,D], proj_context.bias [out_dim] if has_proj_context].
  * 2-D matrices are stored in params.dtype, everything else in F32. */
 
 /* Host-only validation of a blob against params (no GPU needed). */
@@ -193,6 +200,18 @@ JEPA_API void jepa_predictor_destroy(jepa_predictor* pred);
 JEPA_API jepa_status jepa_predict(jepa_predictor* pred, const float* enc_tokens, int n_tokens, const int32_t* ids_ctx,
                          int n_ctx, const int32_t* ids_tgt, int n_tgt, int grid_t, int grid_h, int grid_w,
                          float* out, void* stream);
+/* jepa_predict_ex: the same, with the 2.1 additions ("V-JEPA 2 / 2.1 tensor
+ * maps and RoPE derivation", §3 2.1 predictor forward):
+ *   modality: jepa_modality; selects pred.mod_embed_video or _img, added to
+ *     every row before the blocks (ignored without has_mod_embed);
+ *   out_ctx: device float [n_ctx, out_dim] = pred.proj_context(pred.norm(z))
+ *     [:n_ctx], or NULL; non-NULL needs has_proj_context (else JEPA_ERR_ARG).
+ * jepa_predict is jepa_predict_ex with JEPA_MODALITY_VIDEO and out_ctx NULL,
+ * the default of the pages. */
+JEPA_API jepa_status jepa_predict_ex(jepa_predictor* pred, const float* enc_tokens, int n_tokens,
+                                     const int32_t* ids_ctx, int n_ctx, const int32_t* ids_tgt, int n_tgt,
+                                     int grid_t, int grid_h, int grid_w, int modality, float* out, float* out_ctx,
+                                     void* stream);
 JEPA_API jepa_status jepa_predictor_sync(jepa_predictor* pred, void* stream);
 
 /* ---------------------------------------------------------------- single operations

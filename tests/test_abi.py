@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
         assert n in SIGNATURES, f"binding lacks {n}"
-    assert lib.jepa_abi_version() == 2
+    assert lib.jepa_abi_version() == 3
 
 
 def _blob(cfg):
@@ -117,3 +117,24 @@ def test_argument_errors_without_gpu(lib):
                               100, 0.125, None) == ERR_ARG          # ldv not a multiple of 8
     assert lib.jepa_encoder_sync(None, None) == ERR_ARG
     assert b"NULL" in lib.jepa_last_error()
+
+
+def test_predictor21_blob(lib):
+    """The 2.1 predictor's modality vectors and context projection follow its
+    projection in the blob; params must ask for exactly what the blob holds."""
+    import video_vit_encoder_gb300 as jg
+    from video_vit_encoder_gb300._lib import ERR_BLOB, check
+    import dataclasses
+    pc = dataclasses.replace(synth.PREDICTOR_21, n_layer=1)
+    cfg = synth.CONFIGS["pred21"].with_(predictor=pc)
+    pw = synth.predictor_weights(cfg)
+    order = jg.predictor_tensor_order(pc)
+    assert order[-4:] == [("mod_embed_video", False), ("mod_embed_img", False), ("proj_context.weight", True),
+                          ("proj_context.bias", False)]
+    blob = jg.pack_blob(order, pw, cfg.dtype)
+    p = jg.predictor_params(pc, cfg.dtype)
+    check(lib.jepa_predictor_blob_check(blob, len(blob), C.byref(p)))
+    for field in ("has_mod_embed", "has_proj_context"):
+        q = jg.predictor_params(pc, cfg.dtype)
+        setattr(q, field, 0)
+        assert lib.jepa_predictor_blob_check(blob, len(blob), C.byref(q)) == ERR_BLOB

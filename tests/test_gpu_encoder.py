@@ -146,3 +146,29 @@ def test_normalised_float_input(jg, name):
     for b in range(cfg.batch):
         assert_close_16bit(got[b], oracle.encoder_forward(cfg, w, clip[b])["out"], f"{name} float input clip {b}")
     enc.close()
+
+
+@pytest.mark.parametrize("modality", ["video", "image"])
+def test_small_pred21(jg, modality):
+    """The 2.1 predictor with two blocks on random encoder tokens: both
+    modality vectors, the context projection, ragged row counts."""
+    import dataclasses
+    pc = dataclasses.replace(synth.PREDICTOR_21, n_layer=2)
+    cfg = synth.CONFIGS["pred21"].with_(n_frames=4 if modality == "video" else 1, height=96, width=80,
+                                        predictor=pc)
+    pw = synth.predictor_weights(cfg)
+    rng = np.random.default_rng(7)
+    for k in ("mod_embed_video", "mod_embed_img"):
+        pw[k] = synth.round_to_dtype(rng.standard_normal(pw[k].shape) * 0.5, "f32")
+    grid = cfg.grid()
+    n = grid[0] * grid[1] * grid[2]
+    enc = synth.round_to_dtype(rng.standard_normal((n, 768)), "f32")
+    ctx, tgt = synth.context_target_split(cfg)
+    pred = jg.Predictor(pc, pw, cfg.dtype)
+    out, octx = pred.predict(torch.from_numpy(enc).cuda(), torch.from_numpy(ctx).cuda(), torch.from_numpy(tgt).cuda(),
+                             grid, modality=modality, with_ctx=True)
+    pred.sync()
+    ref = oracle.predictor_outputs(pc, pw, enc.astype(np.float64), ctx, tgt, grid, modality)
+    assert_close_16bit(out.cpu().numpy(), ref["pred"], f"small pred21 {modality}")
+    assert_close_16bit(octx.cpu().numpy(), ref["ctx"], f"small pred21 {modality} ctx")
+    pred.close()

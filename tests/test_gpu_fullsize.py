@@ -177,3 +177,36 @@ def test_img384_end_to_end(jg):
         np.testing.assert_allclose(res["pooled"][b].cpu().numpy(), ref["pooled"],
                                    atol=1e-2 * np.abs(ref["pooled"]).max())
     enc.close()
+
+
+def test_pred21_encoder_and_predictor(jg):
+    """The 2.1 predictor (D384 L12 hd32, interleaved RoPE on the 8 x 24 x 24
+    grid, 8 mask tokens, out 1664, context projection) on the 2.1 ViT-B/16
+    encoder's own output for a 16-frame 384 px clip (4608 tokens): target
+    predictions and context projections end to end against the oracle run on
+    the same encoder tokens, video modality; then the image modality on a
+    576-token image encoded by the same model."""
+    cfg = synth.CONFIGS["pred21"]
+    w = _weights("pred21")
+    pc = cfg.predictor
+    pw = synth.predictor_weights(cfg)
+    enc = jg.Encoder(cfg, w)
+    pred = jg.Predictor(pc, pw, cfg.dtype)
+    for T, mod in ((cfg.n_frames, "video"), (1, "image")):
+        c = cfg.with_(n_frames=T)
+        clip = torch.from_numpy(synth.clip_u8(c, batch=1)).cuda()
+        tokens = enc.encode(clip)["out"][0].contiguous()
+        enc.sync()
+        ctx, tgt = synth.context_target_split(c)
+        out, octx = pred.predict(tokens, torch.from_numpy(ctx).cuda(), torch.from_numpy(tgt).cuda(), c.grid(),
+                                 modality="auto", with_ctx=True)
+        pred.sync()
+        ref = oracle.predictor_outputs(pc, pw, tokens.cpu().numpy().astype(np.float64), ctx, tgt, c.grid(), mod)
+        assert_close_16bit(out.cpu().numpy(), ref["pred"], f"pred21 {mod} targets")
+        assert_close_16bit(octx.cpu().numpy(), ref["ctx"], f"pred21 {mod} context projection")
+        if mod == "video":   # the plain call is the video modality without the context output
+            plain = pred.predict(tokens, torch.from_numpy(ctx).cuda(), torch.from_numpy(tgt).cuda(), c.grid())
+            pred.sync()
+            assert torch.equal(plain, out)
+    pred.close()
+    enc.close()

@@ -18,6 +18,7 @@ STATUS_NAMES = {0: "OK", 1: "ERR_ARG", 2: "ERR_BLOB", 3: "ERR_UNSUPPORTED", 4: "
                 6: "ERR_DEVICE_TIMEOUT"}
 DT_F32, DT_F16, DT_BF16 = 0, 1, 2
 CLIP_U8_THWC, CLIP_F32_CTHW = 0, 1
+MODALITY_VIDEO, MODALITY_IMAGE, MODALITY_AUTO = 0, 1, 2
 
 
 class JepaError(RuntimeError):
@@ -26,7 +27,7 @@ class JepaError(RuntimeError):
         self.status = status
 
 
-ABI_VERSION = 2  # JEPA_ABI_VERSION of include/jepa_gb300.h
+ABI_VERSION = 3  # JEPA_ABI_VERSION of include/jepa_gb300.h
 
 
 class EncoderParams(C.Structure):
@@ -40,7 +41,8 @@ class EncoderParams(C.Structure):
 class PredictorParams(C.Structure):
     _fields_ = [("embed_dim", C.c_int), ("n_layer", C.c_int), ("n_head", C.c_int), ("ffn_dim", C.c_int),
                 ("in_dim", C.c_int), ("out_dim", C.c_int), ("n_mask_tokens", C.c_int), ("mask_index", C.c_int),
-                ("ln_eps", C.c_float), ("rope_theta", C.c_float), ("rope_layout", C.c_int), ("dtype", C.c_int)]
+                ("ln_eps", C.c_float), ("rope_theta", C.c_float), ("rope_layout", C.c_int), ("dtype", C.c_int),
+                ("has_mod_embed", C.c_int), ("has_proj_context", C.c_int)]
 
 
 VP, I, F, ST, U64 = C.c_void_p, C.c_int, C.c_float, C.c_int, C.c_size_t
@@ -62,6 +64,7 @@ SIGNATURES = {
     "jepa_predictor_create": (ST, [VP, U64, C.POINTER(PredictorParams), I, C.POINTER(VP)]),
     "jepa_predictor_destroy": (None, [VP]),
     "jepa_predict": (ST, [VP, VP, I, VP, I, VP, I, I, I, I, VP, VP]),
+    "jepa_predict_ex": (ST, [VP, VP, I, VP, I, VP, I, I, I, I, I, VP, VP, VP]),
     "jepa_predictor_sync": (ST, [VP, VP]),
     "jepa_layernorm_f32": (ST, [VP, VP, VP, VP, I, I, F, VP]),
     "jepa_rope3d_f32": (ST, [VP, I, I, I, I, I, I, I, I, I, I, F, VP]),

@@ -64,6 +64,10 @@ def predictor_tensor_order(pc):
                   (p + "ln2.weight", False), (p + "ln2.bias", False), (p + "ffn_up.weight", True),
                   (p + "ffn_up.bias", False), (p + "ffn_down.weight", True), (p + "ffn_down.bias", False)]
     names += [("norm.weight", False), ("norm.bias", False), ("proj.weight", True), ("proj.bias", False)]
+    if getattr(pc, "has_mod_embed", False):
+        names += [("mod_embed_video", False), ("mod_embed_img", False)]
+    if getattr(pc, "has_proj_context", False):
+        names += [("proj_context.weight", True), ("proj_context.bias", False)]
     return names
 
 
@@ -121,6 +125,8 @@ def predictor_params(pc, dtype: str) -> PredictorParams:
     p.ln_eps, p.rope_theta = pc.ln_eps, pc.rope_theta
     p.rope_layout = LAYOUT_CODE[pc.rope_layout]
     p.dtype = DTYPE_CODE[dtype]
+    p.has_mod_embed = int(bool(getattr(pc, "has_mod_embed", False)))
+    p.has_proj_context = int(bool(getattr(pc, "has_proj_context", False)))
     return p
 
 
@@ -219,7 +225,7 @@ class Encoder:
 
 
 class Predictor:
-    """The V-JEPA 2 masked predictor resident on one GPU."""
+    """The V-JEPA 2 / 2.1 masked predictor resident on one GPU."""
 
     def __init__(self, pcfg, weights: dict, dtype: str, device: int = 0):
         self.lib = load()
@@ -242,13 +248,26 @@ class Predictor:
         except Exception:
             pass
 
-    def predict(self, enc_tokens: torch.Tensor, ids_ctx: torch.Tensor, ids_tgt: torch.Tensor, grid, stream=None):
+    def predict(self, enc_tokens: torch.Tensor, ids_ctx: torch.Tensor, ids_tgt: torch.Tensor, grid, stream=None,
+                modality: str | None = None, with_ctx: bool = False):
+        """Target predictions [n_tgt, out_dim]; with ``with_ctx`` also the
+        context projection [n_ctx, out_dim] (2.1), as ``(pred, ctx)``.
+        modality: None (the plain call: video), "video", "image" or "auto"."""
         out = torch.empty((ids_tgt.numel(), self.pcfg.out_dim), dtype=torch.float32, device=enc_tokens.device)
         gt, gh, gw = grid
-        check(self.lib.jepa_predict(self.handle, _ptr(enc_tokens), enc_tokens.shape[0], _ptr(ids_ctx),
-                                    ids_ctx.numel(), _ptr(ids_tgt), ids_tgt.numel(), gt, gh, gw, _ptr(out),
-                                    _stream(stream)))
-        return out
+        if modality is None and not with_ctx:
+            check(self.lib.jepa_predict(self.handle, _ptr(enc_tokens), enc_tokens.shape[0], _ptr(ids_ctx),
+                                        ids_ctx.numel(), _ptr(ids_tgt), ids_tgt.numel(), gt, gh, gw, _ptr(out),
+                                        _stream(stream)))
+            return out
+        mod = {None: _lib.MODALITY_VIDEO, "video": _lib.MODALITY_VIDEO, "image": _lib.MODALITY_IMAGE,
+               "auto": _lib.MODALITY_AUTO}[modality]
+        ctx = (torch.empty((ids_ctx.numel(), self.pcfg.out_dim), dtype=torch.float32, device=enc_tokens.device)
+               if with_ctx else None)
+        check(self.lib.jepa_predict_ex(self.handle, _ptr(enc_tokens), enc_tokens.shape[0], _ptr(ids_ctx),
+                                       ids_ctx.numel(), _ptr(ids_tgt), ids_tgt.numel(), gt, gh, gw, mod, _ptr(out),
+                                       _ptr(ctx), _stream(stream)))
+        return (out, ctx) if with_ctx else out
 
     def sync(self, stream=None):
         check(self.lib.jepa_predictor_sync(self.handle, _stream(stream)))

@@ -150,6 +150,14 @@ std::vector<Expect> expected_predictor(const jepa_predictor_params& p) {
   v.push_back({DTYPE_F32, D, 1, 1});
   v.push_back({p.dtype, (uint32_t)p.out_dim, D, 2});
   v.push_back({DTYPE_F32, (uint32_t)p.out_dim, 1, 1});
+  if (p.has_mod_embed) {  // 2.1: pred.mod_embed_video, pred.mod_embed_img
+    v.push_back({DTYPE_F32, D, 1, 1});
+    v.push_back({DTYPE_F32, D, 1, 1});
+  }
+  if (p.has_proj_context) {  // 2.1: pred.proj_context
+    v.push_back({p.dtype, (uint32_t)p.out_dim, D, 2});
+    v.push_back({DTYPE_F32, (uint32_t)p.out_dim, 1, 1});
+  }
   return v;
 }
 
@@ -866,6 +874,12 @@ struct jepa_predictor {
   const float *norm_w = nullptr, *norm_b = nullptr;
   const void* w_proj = nullptr;
   const float* b_proj = nullptr;
+  const void* w_projc = nullptr;   // 2.1 context projection, when present
+  const float* b_projc = nullptr;
+  // Per modality (0 video, 1 image): the embed bias and the mask row with the
+  // 2.1 modality vector folded in (the plain ones when the model has none).
+  float* b_emb_mod[2] = {nullptr, nullptr};
+  float* mask_mod[2] = {nullptr, nullptr};
   void* ws = nullptr;
   size_t ws_bytes = 0;
   int* d_status = nullptr;
@@ -902,11 +916,39 @@ jepa_status jepa_predictor_create(const void* blob, size_t blob_bytes, const jep
   pr->norm_b = (const float*)P[i++];
   pr->w_proj = P[i++];
   pr->b_proj = (const float*)P[i++];
-  if (cudaMalloc(&pr->d_status, sizeof(int)) != cudaSuccess) {
+  const float* mods[2] = {nullptr, nullptr};
+  if (params->has_mod_embed) {
+    mods[0] = (const float*)P[i++];
+    mods[1] = (const float*)P[i++];
+  }
+  if (params->has_proj_context) {
+    pr->w_projc = P[i++];
+    pr->b_projc = (const float*)P[i++];
+  }
+  const int D = params->embed_dim;
+  bool ok = cudaMalloc(&pr->d_status, sizeof(int)) == cudaSuccess;
+  for (int m = 0; m < 2 && ok; ++m)
+    ok = cudaMalloc(&pr->b_emb_mod[m], D * sizeof(float)) == cudaSuccess &&
+         cudaMalloc(&pr->mask_mod[m], D * sizeof(float)) == cudaSuccess;
+  if (!ok) {
     jepa_predictor_destroy(pr);
-    return fail(JEPA_ERR_OOM, "predictor status word");
+    return fail(JEPA_ERR_OOM, "predictor: small allocations failed");
   }
   cudaMemset(pr->d_status, 0, sizeof(int));
+  const float* tok = pr->mask_tokens + (size_t)(params->mask_index % params->n_mask_tokens) * D;
+  for (int m = 0; m < 2; ++m) {
+    cudaMemcpy(pr->b_emb_mod[m], pr->b_emb, D * sizeof(float), cudaMemcpyDeviceToDevice);
+    cudaMemcpy(pr->mask_mod[m], tok, D * sizeof(float), cudaMemcpyDeviceToDevice);
+    if (mods[m]) {  // the modality vector joins every row: context rows through the bias, mask rows directly
+      add_vec_kernel<<<(D + 255) / 256, 256>>>(pr->b_emb_mod[m], mods[m], D);
+      add_vec_kernel<<<(D + 255) / 256, 256>>>(pr->mask_mod[m], mods[m], D);
+    }
+  }
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    jepa_predictor_destroy(pr);
+    return fail(JEPA_ERR_CUDA, "predictor create: %s", cudaGetErrorString(e));
+  }
   *out = pr;
   return JEPA_OK;
 }
@@ -919,16 +961,34 @@ void jepa_predictor_destroy(jepa_predictor* pr) {
   cudaFree(pr->ws);
   cudaFree(pr->d_status);
   cudaFree(pr->rope.d);
+  for (int m = 0; m < 2; ++m) {
+    cudaFree(pr->b_emb_mod[m]);
+    cudaFree(pr->mask_mod[m]);
+  }
   delete pr;
 }
 
 jepa_status jepa_predict(jepa_predictor* pr, const float* enc_tokens, int n_tokens, const int32_t* ids_ctx, int n_ctx,
                          const int32_t* ids_tgt, int n_tgt, int grid_t, int grid_h, int grid_w, float* out,
                          void* stream) {
+  return jepa_predict_ex(pr, enc_tokens, n_tokens, ids_ctx, n_ctx, ids_tgt, n_tgt, grid_t, grid_h, grid_w,
+                         JEPA_MODALITY_VIDEO, out, nullptr, stream);
+}
+
+jepa_status jepa_predict_ex(jepa_predictor* pr, const float* enc_tokens, int n_tokens, const int32_t* ids_ctx,
+                            int n_ctx, const int32_t* ids_tgt, int n_tgt, int grid_t, int grid_h, int grid_w,
+                            int modality, float* out, float* out_ctx, void* stream) {
   if (pr == nullptr) return fail(JEPA_ERR_ARG, "predictor handle is NULL");
   if (enc_tokens == nullptr || ids_ctx == nullptr || ids_tgt == nullptr || out == nullptr)
     return fail(JEPA_ERR_ARG, "device buffers are required");
-  if (!aligned16(enc_tokens) || !aligned16(out)) return fail(JEPA_ERR_ARG, "buffers must be 16-byte aligned");
+  if (!aligned16(enc_tokens) || !aligned16(out) || (out_ctx != nullptr && !aligned16(out_ctx)))
+    return fail(JEPA_ERR_ARG, "buffers must be 16-byte aligned");
+  if (modality != JEPA_MODALITY_VIDEO && modality != JEPA_MODALITY_IMAGE && modality != JEPA_MODALITY_AUTO)
+    return fail(JEPA_ERR_ARG, "modality %d", modality);
+  if (out_ctx != nullptr && !pr->p.has_proj_context)
+    return fail(JEPA_ERR_ARG, "out_ctx needs a predictor with a context projection");
+  // AUTO: the image vector for a grid of one temporal slice (the image path's grid)
+  const int mod = modality == JEPA_MODALITY_AUTO ? (grid_t == 1 ? 1 : 0) : (modality == JEPA_MODALITY_IMAGE ? 1 : 0);
   if (n_ctx < 1 || n_tgt < 1 || n_tokens < 1) return fail(JEPA_ERR_ARG, "n_ctx, n_tgt and n_tokens must be >= 1");
   if (grid_t < 1 || grid_h < 1 || grid_w < 1 || (long long)grid_t * grid_h * grid_w != n_tokens)
     return fail(JEPA_ERR_ARG, "grid %dx%dx%d does not hold %d tokens", grid_t, grid_h, grid_w, n_tokens);
@@ -956,12 +1016,11 @@ jepa_status jepa_predict(jepa_predictor* pr, const float* enc_tokens, int n_toke
     Scope sc(pr->prof, P_EMBED, s);
     JEPA_TRY(cuda_status(gather_rows_cast(dt, enc_tokens, ids_ctx, n_ctx, pr->p.in_dim, w.g, s), "gather"));
     EpiParams ep{};
-    ep.bias = pr->b_emb;
+    ep.bias = pr->b_emb_mod[mod];  // embed bias (+ modality vector)
     ep.out = w.x;
     ep.ldo = D;
     JEPA_TRY(run_linear(dt, EPI_F32, w.g, pr->w_emb, n_ctx, D, pr->p.in_dim, ep, pr->d_status, s, pr->sms));
-    const float* tok = pr->mask_tokens + (size_t)(pr->p.mask_index % pr->p.n_mask_tokens) * D;
-    JEPA_TRY(cuda_status(fill_rows(w.x + (size_t)n_ctx * D, tok, n_tgt, D, s), "mask tokens"));
+    JEPA_TRY(cuda_status(fill_rows(w.x + (size_t)n_ctx * D, pr->mask_mod[mod], n_tgt, D, s), "mask tokens"));
   }
   StackDesc sd;
   sd.D = D;
@@ -976,19 +1035,30 @@ jepa_status jepa_predict(jepa_predictor* pr, const float* enc_tokens, int n_toke
   sd.hier_b = nullptr;
   JEPA_TRY(run_blocks(sd, w, 1, n, 0, pr->p.n_layer, pr->rope.rp, w.pos, nullptr, pr->d_status, pr->prof, s,
                       pr->sms));
+  // pred.norm on the target rows (and the context rows when their projection is asked for)
+  const int first = out_ctx != nullptr ? 0 : n_ctx;
   {
     Scope sc(pr->prof, P_LN, s);
-    JEPA_TRY(cuda_status(layernorm(dt, w.x + (size_t)n_ctx * D, pr->norm_w, pr->norm_b, w.y, n_tgt, D,
+    JEPA_TRY(cuda_status(layernorm(dt, w.x + (size_t)first * D, pr->norm_w, pr->norm_b, w.y, n - first, D,
                                    pr->p.ln_eps, s),
                          "layernorm"));
   }
   {
     Scope sc(pr->prof, P_OTHER, s);
+    const size_t esz = dtype_size(dt);
     EpiParams ep{};
     ep.bias = pr->b_proj;
     ep.out = out;
     ep.ldo = pr->p.out_dim;
-    JEPA_TRY(run_linear(dt, EPI_F32, w.y, pr->w_proj, n_tgt, pr->p.out_dim, D, ep, pr->d_status, s, pr->sms));
+    const void* y_tgt = (const char*)w.y + (size_t)(n_ctx - first) * D * esz;
+    JEPA_TRY(run_linear(dt, EPI_F32, y_tgt, pr->w_proj, n_tgt, pr->p.out_dim, D, ep, pr->d_status, s, pr->sms));
+    if (out_ctx != nullptr) {
+      EpiParams ec{};
+      ec.bias = pr->b_projc;
+      ec.out = out_ctx;
+      ec.ldo = pr->p.out_dim;
+      JEPA_TRY(run_linear(dt, EPI_F32, w.y, pr->w_projc, n_ctx, pr->p.out_dim, D, ec, pr->d_status, s, pr->sms));
+    }
   }
   return JEPA_OK;
 }
