@@ -4,7 +4,10 @@
 
 OP is one of attention, qkv, out_proj, ffn_up, ffn_down, layernorm, and
 out_proj_f32 / out_proj_bf16 (the out_proj shape with a plain fp32 or 16-bit
-store instead of the residual add).  Shapes:
+store instead of the residual add), and predictor21: the whole V-JEPA 2.1
+masked predictor (D 384, 12 blocks, head_dim 32, FFN 1536, out 1664, context
+projection) on a 16-frame 384 px clip's 4608 tokens split 2304 / 2304, random
+encoder tokens and weights.  Encoder-op shapes:
 8 clips x 2048 tokens = 16384 rows, D 1024, 16 heads (head_dim 64), FFN 4096,
 bf16 operands.  Inputs are random (the values do not matter for timing).
 Prints the mean time per launch (CUDA events) and the achieved rate.  Used
@@ -37,6 +40,22 @@ def _setup(op):
         vt = rnd(B * H, hd, N)
         out = torch.empty(B, N, D, dtype=bf, device="cuda")
         return (lambda: jb.attention(q, k, vt, B, H, N, hd, out=out)), 4.0 * B * H * N * N * hd, "TFLOP/s"
+    if op == "predictor21":
+        import synth
+        from . import binding
+        pc = synth.PREDICTOR_21
+        cfg = synth.CONFIGS["pred21"]
+        pw = synth.predictor_weights(cfg)
+        grid = cfg.grid()
+        n = grid[0] * grid[1] * grid[2]
+        ctx, tgt = synth.context_target_split(cfg)
+        pred = binding.Predictor(pc, pw, cfg.dtype)
+        enc = torch.randn(n, pc.in_dim, device="cuda", generator=g)
+        ic, it = torch.from_numpy(ctx).cuda(), torch.from_numpy(tgt).cuda()
+        D, F, L = pc.embed_dim, pc.ffn_dim, pc.n_layer
+        fl = (2 * len(ctx) * pc.in_dim * D + L * (2 * n * (4 * D * D + 2 * D * F) + 4 * n * n * D)
+              + 2 * n * D * pc.out_dim)
+        return (lambda: pred.predict(enc, ic, it, grid, modality="video", with_ctx=True)), fl, "TFLOP/s"
     if op == "layernorm":
         x = rnd(M, D, dtype=torch.float32)
         w, b = torch.ones(D, device="cuda"), torch.zeros(D, device="cuda")
@@ -55,7 +74,7 @@ def _setup(op):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("op", choices=["attention", "qkv", "out_proj", "ffn_up", "ffn_down", "layernorm", "out_proj_f32",
-                                   "out_proj_bf16"])
+                                   "out_proj_bf16", "predictor21"])
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args(argv)
