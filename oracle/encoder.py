@@ -287,17 +287,25 @@ def encoder_embed(cfg, wts, clip_u8):
     return x
 
 
-def encoder_forward(cfg, wts, clip_u8, n_layers: int | None = None, return_residual: bool = False):
+def encoder_forward(cfg, wts, clip_u8, n_layers: int | None = None, return_residual: bool = False, keep=None):
     """Encoder forward of ONE clip ``[T, H, W, 3]`` uint8.
 
     Returns dict: ``out`` = enc.norm(x) ``[N, D]`` (last_hidden_state),
     ``hier`` = list of hier_norm.k(x after block hier_layers[k]) ([N] §3,
     [H] Intermediate features), ``pooled`` = token mean of ``out``, and, if
     asked, ``residual`` = x before the final norm.
+
+    ``keep`` (token ids) is the masked encoder forward ([H] Usage, "Predictor";
+    Validation, the masked-encoder row): the embedded tokens are gathered at
+    ``keep`` before the blocks, so attention sees only them, while RoPE keeps
+    each token's true grid position; the rows follow the order of ``keep``.
     """
     T, H, W, _ = clip_u8.shape
     COS, SIN = encoder_rope(cfg, T, H, W)
     x = encoder_embed(cfg, wts, clip_u8)
+    if keep is not None:
+        keep = np.asarray(keep)
+        x, COS, SIN = x[keep], COS[keep], SIN[keep]
     L = cfg.n_layer if n_layers is None else n_layers
     hier = []
     taps = list(getattr(cfg, "hier_layers", ()) or ())

@@ -41,7 +41,7 @@ def _torch_rope(x, pos, layout, theta=10000.0):
     return torch.cat([xr * ang.cos() + rot * ang.sin(), xp], dim=-1)
 
 
-def _torch_encoder(cfg, w, clip):
+def _torch_encoder(cfg, w, clip, keep=None):
     T, H, W, _ = clip.shape
     x = torch.from_numpy(clip.astype(np.float64)).permute(3, 0, 1, 2)
     mean = torch.tensor([0.485, 0.456, 0.406], dtype=torch.float64)[:, None, None, None]
@@ -59,6 +59,9 @@ def _torch_encoder(cfg, w, clip):
     if cfg.rope_interpolate:
         pos[:, 1] = pos[:, 1] * (cfg.rope_ref_grid - 1) / (gh - 1)
         pos[:, 2] = pos[:, 2] * (cfg.rope_ref_grid - 1) / (gw - 1)
+    if keep is not None:                                     # masked encoder: kept tokens, true positions
+        idx = torch.from_numpy(np.asarray(keep)).long()
+        tok, pos = tok[idx], pos[idx]
     h = cfg.n_head
     hier = []
     for i in range(cfg.n_layer):
@@ -290,3 +293,61 @@ def test_predictor21_mask_token_and_modality():
     zv = oracle.predictor_input(pc, pw, enc, ctx, tgt, "video")
     np.testing.assert_allclose(z - zv, np.broadcast_to(pw["mod_embed_img"] - pw["mod_embed_video"], z.shape),
                                atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- masked encoder
+# [H] Usage ("Predictor") and Validation: masks given to the encoder drop the
+# tokens before the blocks; attention sees only the kept ones and RoPE keeps
+# the true positions.
+def _keep_ids(cfg, seed, frac=0.4):
+    n = synth.tokens_per_clip(cfg)
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(n, int(n * frac), replace=False))
+
+
+def test_masked_encoder_matches_torch_composition():
+    cfg = SMALL_21
+    w = _perturb_lns(synth.encoder_weights(cfg), 11)
+    clip = synth.clip_u8(cfg, batch=1)[0]
+    keep = _keep_ids(cfg, 1)
+    got = oracle.encoder_forward(cfg, w, clip, keep=keep)
+    ref, hier = _torch_encoder(cfg, w, clip, keep=keep)
+    assert got["out"].shape == (len(keep), cfg.embed_dim)
+    np.testing.assert_allclose(got["out"], ref, rtol=0, atol=1e-10)
+    for a, b in zip(got["hier"], hier):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-10)
+
+
+def test_masked_encoder_keeping_every_token_is_the_encoder():
+    cfg = SMALL_21
+    w = synth.encoder_weights(cfg)
+    clip = synth.clip_u8(cfg, batch=1)[0]
+    n = synth.tokens_per_clip(cfg)
+    a = oracle.encoder_forward(cfg, w, clip)["out"]
+    b = oracle.encoder_forward(cfg, w, clip, keep=np.arange(n))["out"]
+    np.testing.assert_array_equal(a, b)
+
+
+def test_masked_encoder_is_not_the_gathered_output():
+    """The pages' control: dropping tokens before the blocks differs from
+    gathering the unmasked encoder's output."""
+    cfg = SMALL_21
+    w = synth.encoder_weights(cfg)
+    clip = synth.clip_u8(cfg, batch=1)[0]
+    keep = _keep_ids(cfg, 2)
+    masked = oracle.encoder_forward(cfg, w, clip, keep=keep)["out"]
+    gathered = oracle.encoder_forward(cfg, w, clip)["out"][keep]
+    assert np.abs(masked - gathered).max() > 1e-3
+
+
+def test_masked_encoder_permutation_equivariant_with_true_positions():
+    """Permuting the kept ids permutes the output rows: each token carries its
+    own grid position, not its index in the kept list."""
+    cfg = SMALL_21
+    w = synth.encoder_weights(cfg)
+    clip = synth.clip_u8(cfg, batch=1)[0]
+    keep = _keep_ids(cfg, 3)
+    perm = np.random.default_rng(4).permutation(len(keep))
+    a = oracle.encoder_forward(cfg, w, clip, keep=keep)["out"]
+    b = oracle.encoder_forward(cfg, w, clip, keep=keep[perm])["out"]
+    np.testing.assert_allclose(b, a[perm], atol=1e-11)
