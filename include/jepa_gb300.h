@@ -158,6 +158,18 @@ JEPA_API jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_f
                         int height, int width, float* out_tokens, float* out_pooled, float* out_hier,
                         void* stream);
 
+/* jepa_encode_masked: the masked encoder forward ("V-JEPA 2.1 ViT-B/16 384 -
+ * HuggingFace port", Usage / Predictor and Validation): of each clip only the
+ * n_keep tokens ids_keep[b*n_keep + r] (device int32 [batch, n_keep], ids in
+ * the clip's grid) are embedded and passed through the blocks, so attention
+ * sees only them, while RoPE gives each its true grid position.  Not the same
+ * as gathering jepa_encode's output.  Outputs as jepa_encode with N = n_keep,
+ * rows in the order of ids_keep.  Ids outside the grid are clamped so nothing
+ * is read out of range, and the next sync reports JEPA_ERR_ARG. */
+JEPA_API jepa_status jepa_encode_masked(jepa_encoder* enc, const void* clip, int clip_format, int batch,
+                                        int n_frames, int height, int width, const int32_t* ids_keep, int n_keep,
+                                        float* out_tokens, float* out_pooled, float* out_hier, void* stream);
+
 /* Same computation from and to HOST buffers (pinned memory is fastest): copies
  * the clip to the device, encodes, copies out_tokens (and out_pooled if not
  * NULL) back, and synchronises `stream` before returning. */

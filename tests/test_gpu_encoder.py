@@ -172,3 +172,71 @@ def test_small_pred21(jg, modality):
     assert_close_16bit(out.cpu().numpy(), ref["pred"], f"small pred21 {modality}")
     assert_close_16bit(octx.cpu().numpy(), ref["ctx"], f"small pred21 {modality} ctx")
     pred.close()
+
+
+def _keep(cfg, B, frac, seed):
+    n = synth.tokens_per_clip(cfg)
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.choice(n, int(n * frac), replace=False) for _ in range(B)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("name", ["b21-bf16", "v2-hd32"])
+def test_masked_encoder(jg, name):
+    """Masked encoder forward: each clip keeps its own random 40 % of the
+    tokens (unsorted); every kept row, the taps and the mean against the
+    oracle's masked forward."""
+    cfg = SMALL[name]
+    w = synth.encoder_weights(cfg)
+    clip = synth.clip_u8(cfg)
+    keep = _keep(cfg, cfg.batch, 0.4, 3)
+    enc = jg.Encoder(cfg, w)
+    got = enc.encode_masked(torch.from_numpy(clip).cuda(), torch.from_numpy(keep).cuda(), pooled=True, hier=True)
+    enc.sync()
+    for b in range(cfg.batch):
+        ref = oracle.encoder_forward(cfg, w, clip[b], keep=keep[b])
+        assert_close_16bit(got["out"][b].cpu().numpy(), ref["out"], f"{name} masked clip {b}")
+        for k, tap in enumerate(ref["hier"]):
+            assert_close_16bit(got["hier"][k, b].cpu().numpy(), tap, f"{name} masked tap {k} clip {b}")
+        np.testing.assert_allclose(got["pooled"][b].cpu().numpy(), ref["pooled"],
+                                   atol=1e-2 * np.abs(ref["pooled"]).max())
+    enc.close()
+
+
+def test_masked_encoder_all_tokens_is_permuted_encode(jg):
+    cfg = SMALL["b21-bf16"]
+    w = synth.encoder_weights(cfg)
+    clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
+    n = synth.tokens_per_clip(cfg)
+    perm = np.stack([np.random.default_rng(b).permutation(n) for b in range(cfg.batch)]).astype(np.int32)
+    enc = jg.Encoder(cfg, w)
+    full = enc.encode(clip)["out"].cpu().numpy()
+    got = enc.encode_masked(clip, torch.from_numpy(perm).cuda())["out"].cpu().numpy()
+    enc.sync()
+    for b in range(cfg.batch):
+        np.testing.assert_allclose(got[b], full[b][perm[b]], rtol=0, atol=5e-3 * np.abs(full).max())
+    enc.close()
+
+
+def test_masked_encoder_bad_ids_are_reported_not_read(jg):
+    """Ids outside the grid are clamped by the kernels (no access outside the
+    clip or the tables) and the next sync reports JEPA_ERR_ARG; the handle
+    then works as before."""
+    from video_vit_encoder_gb300._lib import ERR_ARG, JepaError
+    cfg = SMALL["v2-hd32"]
+    w = synth.encoder_weights(cfg)
+    clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
+    n = synth.tokens_per_clip(cfg)
+    keep = _keep(cfg, cfg.batch, 0.3, 5)
+    bad = keep.copy()
+    bad[0, 3] = n + 5
+    bad[1, 0] = -3
+    enc = jg.Encoder(cfg, w)
+    enc.encode_masked(clip, torch.from_numpy(bad).cuda())
+    with pytest.raises(JepaError) as e:
+        enc.sync()
+    assert e.value.status == ERR_ARG
+    got = enc.encode_masked(clip, torch.from_numpy(keep).cuda())["out"].cpu().numpy()
+    enc.sync()
+    ref = oracle.encoder_forward(cfg, w, clip[1].cpu().numpy(), keep=keep[1])
+    assert_close_16bit(got[1], ref["out"], "after a bad-id call")
+    enc.close()

@@ -210,3 +210,21 @@ def test_pred21_encoder_and_predictor(jg):
             assert torch.equal(plain, out)
     pred.close()
     enc.close()
+
+
+def test_c3_masked_encoder_clip0(jg):
+    """Masked encoder forward at the ViT-L/16 16 x 256 x 256 geometry, batch 8,
+    each clip keeping its own random half of the 2048 tokens; clip 0 end to end
+    against the oracle's masked forward."""
+    cfg = synth.CONFIGS["c3"]
+    w = _weights("c3")
+    clip = synth.clip_u8(cfg)
+    n = synth.tokens_per_clip(cfg)
+    keep = np.stack([np.random.default_rng(40 + b).choice(n, n // 2, replace=False)
+                     for b in range(cfg.batch)]).astype(np.int32)
+    enc = jg.Encoder(cfg, w)
+    got = enc.encode_masked(torch.from_numpy(clip).cuda(), torch.from_numpy(keep).cuda())["out"]
+    enc.sync()
+    ref = oracle.encoder_forward(cfg, w, clip[0], keep=keep[0])
+    assert_close_16bit(got[0].cpu().numpy(), ref["out"], "c3 masked clip 0")
+    enc.close()

@@ -513,7 +513,8 @@ jepa_status read_status(int* d_status, cudaStream_t s) {
   CUDA_TRY(cudaMemcpy(&h, d_status, sizeof(int), cudaMemcpyDeviceToHost));
   if (h != 0) {
     CUDA_TRY(cudaMemset(d_status, 0, sizeof(int)));
-    return fail(JEPA_ERR_DEVICE_TIMEOUT, "a kernel gave up waiting on a barrier (status 0x%x)", h);
+    if (h & DEV_TIMEOUT) return fail(JEPA_ERR_DEVICE_TIMEOUT, "a kernel gave up waiting on a barrier (status 0x%x)", h);
+    return fail(JEPA_ERR_ARG, "token ids outside the grid (clamped; results invalid) (status 0x%x)", h);
   }
   return JEPA_OK;
 }
@@ -610,15 +611,19 @@ StackDesc enc_stack(const jepa_encoder* enc) {
   return sd;
 }
 
+// Patch embedding of every token, or (keep != nullptr) of the n_keep tokens
+// keep[b * n_keep + r] of each clip b, in that order (the masked encoder).
 jepa_status embed_into(jepa_encoder* enc, Work& w, const void* clip, int fmt, int batch, int T, int H, int W,
-                       const Geom& g, float* x_out, cudaStream_t s) {
+                       const Geom& g, float* x_out, cudaStream_t s, const int* keep = nullptr, int n_keep = 0) {
   const int D = enc->p.embed_dim, dt = enc->p.dtype;
-  const int M = batch * g.n_tok;
+  const int M = batch * (keep != nullptr ? n_keep : g.n_tok);
   Scope sc(enc->prof, P_EMBED, s);
   if (fmt == JEPA_CLIP_U8_THWC)
-    JEPA_TRY(cuda_status(unfold_clip_u8(dt, (const uint8_t*)clip, w.g, batch, T, H, W, g.tub, s), "unfold"));
+    JEPA_TRY(cuda_status(unfold_clip_u8(dt, (const uint8_t*)clip, w.g, batch, T, H, W, g.tub, s, keep, n_keep),
+                         "unfold"));
   else
-    JEPA_TRY(cuda_status(unfold_clip_f32(dt, (const float*)clip, w.g, batch, T, H, W, g.tub, s), "unfold"));
+    JEPA_TRY(cuda_status(unfold_clip_f32(dt, (const float*)clip, w.g, batch, T, H, W, g.tub, s, keep, n_keep),
+                         "unfold"));
   const bool img = g.tub == 1;
   EpiParams ep{};
   ep.bias = img ? enc->b_pe_img : enc->b_pe;
@@ -788,6 +793,45 @@ jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_format, in
   if (out_pooled != nullptr) {
     Scope sc(enc->prof, P_OTHER, s);
     JEPA_TRY(cuda_status(mean_pool(out_tokens, out_pooled, batch, g.n_tok, D, s), "mean pool"));
+  }
+  return JEPA_OK;
+}
+
+jepa_status jepa_encode_masked(jepa_encoder* enc, const void* clip, int clip_format, int batch, int n_frames,
+                               int height, int width, const int32_t* ids_keep, int n_keep, float* out_tokens,
+                               float* out_pooled, float* out_hier, void* stream) {
+  Geom g;
+  JEPA_TRY(check_clip(enc, batch, n_frames, height, width, g));
+  if (clip == nullptr || out_tokens == nullptr || ids_keep == nullptr)
+    return fail(JEPA_ERR_ARG, "clip, ids_keep and out_tokens are required");
+  if (n_keep < 1 || n_keep > g.n_tok) return fail(JEPA_ERR_ARG, "n_keep %d must be in 1..%d", n_keep, g.n_tok);
+  if (!aligned16(clip) || !aligned16(out_tokens) || !aligned16(out_pooled) || !aligned16(out_hier))
+    return fail(JEPA_ERR_ARG, "device buffers must be 16-byte aligned");
+  if (clip_format != JEPA_CLIP_U8_THWC && clip_format != JEPA_CLIP_F32_CTHW)
+    return fail(JEPA_ERR_ARG, "clip_format %d", clip_format);
+  cudaStream_t s = (cudaStream_t)stream;
+  CUDA_TRY(cudaSetDevice(enc->device));
+  Geom gk = g;  // the blocks see n_keep tokens per clip
+  gk.n_tok = n_keep;
+  JEPA_TRY(ensure_ws(enc, batch, gk));
+  const int hd = enc->p.embed_dim / enc->p.n_head;
+  // RoPE tables for the full grid: each kept token keeps its own grid cell
+  JEPA_TRY(rope_prepare(enc->rope, hd, enc->p.rope_layout, enc->p.rope_theta, g.gt, g.gh, g.gw,
+                        enc->p.rope_interpolate, enc->p.rope_ref_grid, s));
+  Work w = carve(enc->ws, enc->p.dtype, batch, n_keep, enc->p.embed_dim, enc->p.ffn_dim, 1536, false);
+  JEPA_TRY(cuda_status(check_ids(ids_keep, (long)batch * n_keep, g.n_tok, enc->d_status, s), "id check"));
+  JEPA_TRY(embed_into(enc, w, clip, clip_format, batch, n_frames, height, width, g, w.x, s, ids_keep, n_keep));
+  JEPA_TRY(run_blocks(enc_stack(enc), w, batch, n_keep, 0, enc->p.n_layer, enc->rope.rp, ids_keep, out_hier,
+                      enc->d_status, enc->prof, s, enc->sms));
+  const int M = batch * n_keep, D = enc->p.embed_dim;
+  {
+    Scope sc(enc->prof, P_LN, s);
+    JEPA_TRY(cuda_status(layernorm(DTYPE_F32, w.x, enc->norm_w, enc->norm_b, out_tokens, M, D, enc->p.ln_eps, s),
+                         "final layernorm"));
+  }
+  if (out_pooled != nullptr) {
+    Scope sc(enc->prof, P_OTHER, s);
+    JEPA_TRY(cuda_status(mean_pool(out_tokens, out_pooled, batch, n_keep, D, s), "mean pool"));
   }
   return JEPA_OK;
 }
@@ -1014,7 +1058,9 @@ jepa_status jepa_predict_ex(jepa_predictor* pr, const float* enc_tokens, int n_t
   CUDA_TRY(cudaMemcpyAsync(w.pos + n_ctx, ids_tgt, sizeof(int) * n_tgt, cudaMemcpyDeviceToDevice, s));
   {
     Scope sc(pr->prof, P_EMBED, s);
-    JEPA_TRY(cuda_status(gather_rows_cast(dt, enc_tokens, ids_ctx, n_ctx, pr->p.in_dim, w.g, s), "gather"));
+    JEPA_TRY(cuda_status(check_ids(ids_ctx, n_ctx, n_tokens, pr->d_status, s), "id check"));
+    JEPA_TRY(cuda_status(check_ids(ids_tgt, n_tgt, n_tokens, pr->d_status, s), "id check"));
+    JEPA_TRY(cuda_status(gather_rows_cast(dt, enc_tokens, n_tokens, ids_ctx, n_ctx, pr->p.in_dim, w.g, s), "gather"));
     EpiParams ep{};
     ep.bias = pr->b_emb_mod[mod];  // embed bias (+ modality vector)
     ep.out = w.x;

@@ -13,7 +13,9 @@ namespace jepa {
 
 // ----------------------------------------------------------------------------- status word
 // Bits set by a kernel in the handle's device status word.
-enum : int { DEV_TIMEOUT = 1 };
+// Device status bits: a bounded wait expired; a token id was outside its grid
+// (the kernels clamp it so nothing is read out of range).
+enum : int { DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
 // A wait on a barrier gives up after this many nanoseconds (a correct kernel
 // never waits more than microseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

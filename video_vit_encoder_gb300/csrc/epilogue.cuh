@@ -83,8 +83,9 @@ __device__ __forceinline__ void epilogue_apply(const EpiParams& ep, int row, int
     const int tok = row - clip * ep.n_tok;
     const size_t bh = (size_t)clip * ep.n_head + head;
     if (which < 2) {
-      const int gid = ep.pos_ids != nullptr ? __ldg(ep.pos_ids + row) : tok;
       const int plane = ep.rope.gh * ep.rope.gw;
+      // a caller's id outside the grid is clamped (and reported by the id check)
+      const int gid = min(max(ep.pos_ids != nullptr ? __ldg(ep.pos_ids + row) : tok, 0), ep.rope.gt * plane - 1);
       const int t = gid / plane;
       const int rem = gid - t * plane;
       const int h = rem / ep.rope.gw;

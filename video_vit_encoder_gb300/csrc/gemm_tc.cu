@@ -64,8 +64,9 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
   if (which < 2) {
     int p[3] = {0, 0, 0};
     if (row_ok) {
-      const int gid = ep.pos_ids != nullptr ? __ldg(ep.pos_ids + row) : tok;
       const int plane = ep.rope.gh * ep.rope.gw;
+      // a caller's id outside the grid is clamped (and reported by the id check)
+      const int gid = min(max(ep.pos_ids != nullptr ? __ldg(ep.pos_ids + row) : tok, 0), ep.rope.gt * plane - 1);
       p[0] = gid / plane;
       const int rem = gid - p[0] * plane;
       p[1] = rem / ep.rope.gw;

@@ -34,17 +34,22 @@ cudaError_t attention_simt(int dtype, const void* q, const void* k, const void* 
 
 // Element-wise / row-wise kernels.
 // tubelet 2 (clips) or 1 (the 2.1 image path): rows of 3 * tubelet * 256.
+// keep (device [batch, n_keep] token ids, clamped to the grid): only those
+// tokens, in that order (the masked encoder); nullptr: every token.
 cudaError_t unfold_clip_u8(int dtype, const uint8_t* clip, void* out, int batch, int T, int H, int W, int tubelet,
-                           cudaStream_t s);
+                           cudaStream_t s, const int* keep = nullptr, int n_keep = 0);
 cudaError_t unfold_clip_f32(int dtype, const float* clip, void* out, int batch, int T, int H, int W, int tubelet,
-                            cudaStream_t s);
+                            cudaStream_t s, const int* keep = nullptr, int n_keep = 0);
 cudaError_t layernorm(int out_dtype, const float* x, const float* w, const float* b, void* y, int rows, int dim,
                       float eps, cudaStream_t s);
 cudaError_t mean_pool(const float* x, float* out, int batch, int n_tok, int dim, cudaStream_t s);
 cudaError_t rope_inplace_f32(float* x, int batch, int n_tok, int n_head, int head_dim, const RopeParams& rp,
                              cudaStream_t s);
-cudaError_t gather_rows_cast(int dtype, const float* src, const int* ids, int n, int dim, void* dst,
+// dst row r = src row ids[r] cast to dtype; ids are clamped to [0, n_src).
+cudaError_t gather_rows_cast(int dtype, const float* src, int n_src, const int* ids, int n, int dim, void* dst,
                              cudaStream_t s);
+// Sets DEV_BAD_INDEX in *status when any of the n ids lies outside [0, limit).
+cudaError_t check_ids(const int* ids, long n, int limit, int* status, cudaStream_t s);
 cudaError_t fill_rows(float* dst, const float* row, int n, int dim, cudaStream_t s);
 cudaError_t add_row_vector(float* x, const float* v, int rows, int dim, cudaStream_t s);
 cudaError_t wait_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t s);

@@ -17,21 +17,24 @@ __constant__ float c_std255[3] = {255.0f * 0.229f, 255.0f * 0.224f, 255.0f * 0.2
 // tubelet row (48 contiguous bytes of the THWC clip) and writes the three
 // 16-wide runs c*(TUB*256) + dt*256 + y*16 + [0,16) of the token's
 // 3*TUB*256-wide row (the row-major C,T,H,W flattening of the Conv3d kernel,
-// conversion notes §2).  TUB = 2 for clips, 1 for the 2.1 image path.
+// conversion notes §2).  TUB = 2 for clips, 1 for the 2.1 image path.  With
+// `keep` ([batch, n_keep] token ids, the masked encoder) row r of clip b is
+// token keep[b * n_keep + r], clamped to the grid.
 template <typename T, int TUB>
 __global__ void unfold_u8_kernel(const uint8_t* __restrict__ clip, T* __restrict__ out, int batch, int T_, int H,
-                                 int W) {
+                                 int W, const int* __restrict__ keep, int n_keep) {
   constexpr int K = 3 * TUB * 256;
   const int gt = T_ / TUB, gh = H >> 4, gw = W >> 4;
   const long n_tok = (long)gt * gh * gw;
+  const long rows = keep != nullptr ? n_keep : n_tok;  // rows per clip
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long total = (long)batch * n_tok * 16 * TUB;
+  const long total = (long)batch * rows * 16 * TUB;
   if (idx >= total) return;
   const int y = idx & 15;
   const int dt = (int)((idx >> 4) % TUB);
   const long row = (idx >> 4) / TUB;
-  const long b = row / n_tok;
-  const long tok = row - b * n_tok;
+  const long b = row / rows;
+  const long tok = keep != nullptr ? min(max(__ldg(keep + row), 0), (int)n_tok - 1) : row - b * rows;
   const int t = tok / (gh * gw);
   const int rem = tok - (long)t * gh * gw;
   const int hh = rem / gw, ww = rem - hh * gw;
@@ -69,20 +72,21 @@ __global__ void unfold_u8_kernel(const uint8_t* __restrict__ clip, T* __restrict
 // one thread per (token, c, dt, y) copies 16 floats.
 template <typename T, int TUB>
 __global__ void unfold_f32_kernel(const float* __restrict__ clip, T* __restrict__ out, int batch, int T_, int H,
-                                  int W) {
+                                  int W, const int* __restrict__ keep, int n_keep) {
   constexpr int K = 3 * TUB * 256;
   const int gt = T_ / TUB, gh = H >> 4, gw = W >> 4;
   const long n_tok = (long)gt * gh * gw;
+  const long rows = keep != nullptr ? n_keep : n_tok;  // rows per clip
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long total = (long)batch * n_tok * 48 * TUB;
+  const long total = (long)batch * rows * 48 * TUB;
   if (idx >= total) return;
   const int y = idx & 15;
   const int dt = (int)((idx >> 4) % TUB);
   const long r2 = (idx >> 4) / TUB;
   const int c = r2 % 3;
   const long row = r2 / 3;
-  const long b = row / n_tok;
-  const long tok = row - b * n_tok;
+  const long b = row / rows;
+  const long tok = keep != nullptr ? min(max(__ldg(keep + row), 0), (int)n_tok - 1) : row - b * rows;
   const int t = tok / (gh * gw);
   const int rem = tok - (long)t * gh * gw;
   const int hh = rem / gw, ww = rem - hh * gw;
@@ -210,16 +214,26 @@ __global__ void rope_f32_kernel(float* __restrict__ x, int rows, int n_tok, int 
 }
 
 template <typename T>
-__global__ void gather_cast_kernel(const float* __restrict__ src, const int* __restrict__ ids, int n, int dim,
-                                   T* __restrict__ dst) {
+__global__ void gather_cast_kernel(const float* __restrict__ src, int n_src, const int* __restrict__ ids, int n,
+                                   int dim, T* __restrict__ dst) {
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
   const int q = dim >> 2;
   if (idx >= (long)n * q) return;
   const long r = idx / q;
   const int c = (idx - r * q) * 4;
-  const float4 v = __ldg(reinterpret_cast<const float4*>(src + (size_t)__ldg(ids + r) * dim + c));
+  const int id = min(max(__ldg(ids + r), 0), n_src - 1);  // out-of-range ids are clamped (and reported)
+  const float4 v = __ldg(reinterpret_cast<const float4*>(src + (size_t)id * dim + c));
   T* d = dst + r * dim + c;
   d[0] = DT<T>::from(v.x); d[1] = DT<T>::from(v.y); d[2] = DT<T>::from(v.z); d[3] = DT<T>::from(v.w);
+}
+
+// Sets DEV_BAD_INDEX when any id lies outside [0, limit).
+__global__ void check_ids_kernel(const int* __restrict__ ids, long n, int limit, int* status) {
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    const int v = __ldg(ids + i);
+    if (v < 0 || v >= limit) atomicOr(status, DEV_BAD_INDEX);
+  }
 }
 
 __global__ void fill_rows_kernel(float* __restrict__ dst, const float* __restrict__ row, int n, int dim) {
@@ -243,39 +257,48 @@ inline unsigned grid_for(long n, int block) { return (unsigned)((n + block - 1) 
 }  // namespace
 
 template <int TUB>
-cudaError_t unfold_u8_t(int dtype, const uint8_t* clip, void* out, int batch, int T, int H, int W, cudaStream_t s) {
-  const long total = (long)batch * (T / TUB) * (H / 16) * (W / 16) * 16 * TUB;
+cudaError_t unfold_u8_t(int dtype, const uint8_t* clip, void* out, int batch, int T, int H, int W, const int* keep,
+                        int n_keep, cudaStream_t s) {
+  const long rows = keep != nullptr ? n_keep : (long)(T / TUB) * (H / 16) * (W / 16);
+  const long total = (long)batch * rows * 16 * TUB;
+  if (total == 0) return cudaSuccess;
   if (dtype == DTYPE_BF16)
-    unfold_u8_kernel<__nv_bfloat16, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__nv_bfloat16*)out, batch, T, H, W);
+    unfold_u8_kernel<__nv_bfloat16, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__nv_bfloat16*)out, batch, T, H, W,
+                                                                              keep, n_keep);
   else if (dtype == DTYPE_F16)
-    unfold_u8_kernel<__half, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__half*)out, batch, T, H, W);
+    unfold_u8_kernel<__half, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__half*)out, batch, T, H, W, keep, n_keep);
   else
-    unfold_u8_kernel<float, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (float*)out, batch, T, H, W);
+    unfold_u8_kernel<float, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (float*)out, batch, T, H, W, keep, n_keep);
   return cudaGetLastError();
 }
 
 template <int TUB>
-cudaError_t unfold_f32_t(int dtype, const float* clip, void* out, int batch, int T, int H, int W, cudaStream_t s) {
-  const long total = (long)batch * (T / TUB) * (H / 16) * (W / 16) * 48 * TUB;
+cudaError_t unfold_f32_t(int dtype, const float* clip, void* out, int batch, int T, int H, int W, const int* keep,
+                         int n_keep, cudaStream_t s) {
+  const long rows = keep != nullptr ? n_keep : (long)(T / TUB) * (H / 16) * (W / 16);
+  const long total = (long)batch * rows * 48 * TUB;
+  if (total == 0) return cudaSuccess;
   if (dtype == DTYPE_BF16)
-    unfold_f32_kernel<__nv_bfloat16, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__nv_bfloat16*)out, batch, T, H, W);
+    unfold_f32_kernel<__nv_bfloat16, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__nv_bfloat16*)out, batch, T, H,
+                                                                               W, keep, n_keep);
   else if (dtype == DTYPE_F16)
-    unfold_f32_kernel<__half, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__half*)out, batch, T, H, W);
+    unfold_f32_kernel<__half, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (__half*)out, batch, T, H, W, keep,
+                                                                        n_keep);
   else
-    unfold_f32_kernel<float, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (float*)out, batch, T, H, W);
+    unfold_f32_kernel<float, TUB><<<grid_for(total, 256), 256, 0, s>>>(clip, (float*)out, batch, T, H, W, keep, n_keep);
   return cudaGetLastError();
 }
 
 cudaError_t unfold_clip_u8(int dtype, const uint8_t* clip, void* out, int batch, int T, int H, int W, int tubelet,
-                           cudaStream_t s) {
-  return tubelet == 1 ? unfold_u8_t<1>(dtype, clip, out, batch, T, H, W, s)
-                      : unfold_u8_t<2>(dtype, clip, out, batch, T, H, W, s);
+                           cudaStream_t s, const int* keep, int n_keep) {
+  return tubelet == 1 ? unfold_u8_t<1>(dtype, clip, out, batch, T, H, W, keep, n_keep, s)
+                      : unfold_u8_t<2>(dtype, clip, out, batch, T, H, W, keep, n_keep, s);
 }
 
 cudaError_t unfold_clip_f32(int dtype, const float* clip, void* out, int batch, int T, int H, int W, int tubelet,
-                            cudaStream_t s) {
-  return tubelet == 1 ? unfold_f32_t<1>(dtype, clip, out, batch, T, H, W, s)
-                      : unfold_f32_t<2>(dtype, clip, out, batch, T, H, W, s);
+                            cudaStream_t s, const int* keep, int n_keep) {
+  return tubelet == 1 ? unfold_f32_t<1>(dtype, clip, out, batch, T, H, W, keep, n_keep, s)
+                      : unfold_f32_t<2>(dtype, clip, out, batch, T, H, W, keep, n_keep, s);
 }
 
 cudaError_t layernorm(int out_dtype, const float* x, const float* w, const float* b, void* y, int rows, int dim,
@@ -308,16 +331,23 @@ cudaError_t rope_inplace_f32(float* x, int batch, int n_tok, int n_head, int hea
   return cudaGetLastError();
 }
 
-cudaError_t gather_rows_cast(int dtype, const float* src, const int* ids, int n, int dim, void* dst,
+cudaError_t gather_rows_cast(int dtype, const float* src, int n_src, const int* ids, int n, int dim, void* dst,
                              cudaStream_t s) {
   const long total = (long)n * (dim / 4);
   if (total == 0) return cudaSuccess;
   if (dtype == DTYPE_BF16)
-    gather_cast_kernel<__nv_bfloat16><<<grid_for(total, 256), 256, 0, s>>>(src, ids, n, dim, (__nv_bfloat16*)dst);
+    gather_cast_kernel<__nv_bfloat16><<<grid_for(total, 256), 256, 0, s>>>(src, n_src, ids, n, dim,
+                                                                           (__nv_bfloat16*)dst);
   else if (dtype == DTYPE_F16)
-    gather_cast_kernel<__half><<<grid_for(total, 256), 256, 0, s>>>(src, ids, n, dim, (__half*)dst);
+    gather_cast_kernel<__half><<<grid_for(total, 256), 256, 0, s>>>(src, n_src, ids, n, dim, (__half*)dst);
   else
-    gather_cast_kernel<float><<<grid_for(total, 256), 256, 0, s>>>(src, ids, n, dim, (float*)dst);
+    gather_cast_kernel<float><<<grid_for(total, 256), 256, 0, s>>>(src, n_src, ids, n, dim, (float*)dst);
+  return cudaGetLastError();
+}
+
+cudaError_t check_ids(const int* ids, long n, int limit, int* status, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  check_ids_kernel<<<grid_for(n, 256), 256, 0, s>>>(ids, n, limit, status);
   return cudaGetLastError();
 }
 
