@@ -36,15 +36,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 UNIT = "tokens/s"
-# name -> (seeded config, metric, workload description)
+# name -> (seeded config, metric, workload description, fraction of tokens kept or None)
 WORKLOADS = {
     "vitl16-16f256": ("c3", "encoder tokens/sec (ViT-L/16, 16f 256px, bf16) and % of bf16 tensor peak",
                       "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 16f x 256x256 (2048 tokens/clip), "
-                      "batch 8 per GPU"),
+                      "batch 8 per GPU", None),
+    "vitl16-16f256-masked50": ("c3", "masked-encoder kept tokens/sec (ViT-L/16, 16f 256px, half the tokens kept, "
+                               "bf16) and % of bf16 tensor peak",
+                               "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 16f x 256x256, masked encoder "
+                               "forward keeping a seeded random 1024 of each clip's 2048 tokens, batch 8 per GPU", 0.5),
     "vitb16-img384": ("img384", "encoder tokens/sec (V-JEPA 2.1 ViT-B/16 native image path, 384px, bf16) and % of "
                       "bf16 tensor peak",
                       "ViT-B/16 12L D768 h12 FFN3072, bf16, 2.1 native image path (tubelet 1, patch_embed_img), "
-                      "interleaved interpolated RoPE, 1f x 384x384 (576 tokens/image), batch 32 per GPU"),
+                      "interleaved interpolated RoPE, 1f x 384x384 (576 tokens/image), batch 32 per GPU", None),
 }
 DEFAULT_WORKLOAD = "vitl16-16f256"
 CLASSES = ["patch_embed", "layernorm", "qkv_gemm", "attention", "out_proj_gemm", "ffn_up_gemm", "ffn_down_gemm",
@@ -95,8 +99,9 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)   # nvidia-smi is sampling before the timed region starts
         except OSError:
             self.proc = None
         return self
@@ -209,7 +214,10 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    key, metric, workload = WORKLOADS[args.workload]
+    key, metric, workload, keep_frac = WORKLOADS[args.workload]
+    if keep_frac is not None:
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the unmasked workloads only"}))
+        return 0
     cfg = synth.CONFIGS[key]
     w = synth.encoder_weights(cfg)
     clip = synth.clip_u8(cfg, batch=1)[0]
@@ -236,7 +244,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -263,10 +271,12 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    key, metric, workload = WORKLOADS[args.workload]
+    key, metric, workload, keep_frac = WORKLOADS[args.workload]
     cfg = synth.CONFIGS[key]
     B = cfg.batch
-    n_tok = synth.tokens_per_clip(cfg)
+    n_grid = synth.tokens_per_clip(cfg)
+    # tokens per clip that pass through the blocks (all, or the kept ones)
+    n_tok = n_grid if keep_frac is None else int(n_grid * keep_frac)
     weights = synth.encoder_weights(cfg)
     # each rank encodes its own clips (clip streams rank*B .. rank*B+B-1)
     clip_np = synth.clip_u8(cfg, batch=B, first_clip=first_clip_for_rank(rank, B))
@@ -275,9 +285,18 @@ def main():
     out = torch.empty((B, n_tok, cfg.embed_dim), dtype=torch.float32, device="cuda")
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
+    if keep_frac is None:
+        def step():
+            enc.encode(clip, out=out)
+    else:
+        keep = torch.from_numpy(np.stack([np.random.default_rng(1000 + b).choice(n_grid, n_tok, replace=False)
+                                          for b in range(B)]).astype(np.int32)).cuda()
+
+        def step():
+            return enc.encode_masked(clip, keep)["out"]
 
     for _ in range(args.warmup):
-        enc.encode(clip, out=out)
+        step()
     enc.sync()
     enc.profile(reset=True)
     enc.set_profiling(True)
@@ -291,7 +310,7 @@ def main():
         for i in range(args.steps):
             flush.fill_(float(i))                     # L2 flush, outside the timed region
             starts[i].record(stream)
-            enc.encode(clip, out=out)
+            step()
             ends[i].record(stream)
         torch.cuda.synchronize()
     enc.sync()
@@ -325,11 +344,19 @@ def main():
     # end to end through the host-buffer entry point (pinned host memory)
     hclip = torch.from_numpy(clip_np).pin_memory()
     hout = torch.empty((B, n_tok, cfg.embed_dim), dtype=torch.float32).pin_memory()
-    enc.encode_host(hclip, hout)
+
+    def e2e_step():
+        if keep_frac is None:
+            enc.encode_host(hclip, hout)
+        else:   # the masked forward has no host entry point: copies around jepa_encode_masked
+            clip.copy_(hclip, non_blocking=True)
+            hout.copy_(step(), non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+    e2e_step()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
-        enc.encode_host(hclip, hout)
+        e2e_step()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, dist, "cuda")
     e2e_val = world * B * n_tok / e2e_s
 
@@ -347,7 +374,9 @@ def main():
         "kernels": kernels,
         "gpu_launches": gpu_launches,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(hclip.numel()),
-                "d2h_bytes_per_step": int(hout.numel() * 4), "api": "jepa_encode_host (pinned host buffers)"},
+                "d2h_bytes_per_step": int(hout.numel() * 4),
+                "api": "jepa_encode_host (pinned host buffers)" if keep_frac is None else
+                       "pinned host clip -> device, jepa_encode_masked, device -> pinned host tokens"},
         "clocks": clocks.summary(),
     }
     if args.workload == DEFAULT_WORKLOAD:

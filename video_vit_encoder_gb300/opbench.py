@@ -52,9 +52,9 @@ def _setup(op):
         pred = binding.Predictor(pc, pw, cfg.dtype)
         enc = torch.randn(n, pc.in_dim, device="cuda", generator=g)
         ic, it = torch.from_numpy(ctx).cuda(), torch.from_numpy(tgt).cuda()
-        D, F, L = pc.embed_dim, pc.ffn_dim, pc.n_layer
-        fl = (2 * len(ctx) * pc.in_dim * D + L * (2 * n * (4 * D * D + 2 * D * F) + 4 * n * n * D)
-              + 2 * n * D * pc.out_dim)
+        pd, pf, pl = pc.embed_dim, pc.ffn_dim, pc.n_layer
+        fl = (2 * len(ctx) * pc.in_dim * pd + pl * (2 * n * (4 * pd * pd + 2 * pd * pf) + 4 * n * n * pd)
+              + 2 * n * pd * pc.out_dim)
         return (lambda: pred.predict(enc, ic, it, grid, modality="video", with_ctx=True)), fl, "TFLOP/s"
     if op == "layernorm":
         x = rnd(M, D, dtype=torch.float32)
