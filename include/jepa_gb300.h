@@ -158,6 +158,17 @@ JEPA_API jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_f
                         int height, int width, float* out_tokens, float* out_pooled, float* out_hier,
                         void* stream);
 
+/* jepa_encoder_set_graphs: replay of repeated jepa_encode calls (on by
+ * default).  A call whose shapes and buffers equal an earlier call's runs as
+ * one CUDA graph launch on `stream`: the first such call runs eagerly, the
+ * second is captured (on a stream private to the handle) and later ones
+ * replay it, so the host issues one launch instead of one per kernel and the
+ * kernels follow each other without launch gaps.  The handle keeps graphs
+ * for the 8 most recent signatures; a workspace reallocation drops them.
+ * Calls made while profiling is on always run eagerly.  on = 0 turns replay
+ * off. */
+JEPA_API jepa_status jepa_encoder_set_graphs(jepa_encoder* enc, int on);
+
 /* jepa_encode_masked: the masked encoder forward ("V-JEPA 2.1 ViT-B/16 384 -
  * HuggingFace port", Usage / Predictor and Validation): of each clip only the
  * n_keep tokens ids_keep[b*n_keep + r] (device int32 [batch, n_keep], ids in

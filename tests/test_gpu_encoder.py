@@ -240,3 +240,38 @@ def test_masked_encoder_bad_ids_are_reported_not_read(jg):
     ref = oracle.encoder_forward(cfg, w, clip[1].cpu().numpy(), keep=keep[1])
     assert_close_16bit(got[1], ref["out"], "after a bad-id call")
     enc.close()
+
+
+def test_graph_replay_matches_eager(jg):
+    """Repeated calls replay a captured graph: outputs equal the eager run
+    bit for bit, through shape changes (the RoPE tables are shared), a
+    workspace reallocation, and new contents in the same input buffer."""
+    base = SMALL["b21-bf16"]
+    w = synth.encoder_weights(base)
+    enc = jg.Encoder(base, w)
+    shapes = [base, base.with_(n_frames=6, height=64, width=96), base.with_(batch=1)]
+    clips = {i: torch.from_numpy(synth.clip_u8(c)).cuda() for i, c in enumerate(shapes)}
+    enc.set_graphs(False)
+    ref = {i: enc.encode(clips[i], pooled=True)["out"].clone() for i in clips}
+    enc.sync()
+    enc.set_graphs(True)
+    outs = {i: torch.empty_like(ref[i]) for i in clips}
+    for i in [0, 0, 1, 0, 1, 1, 2, 0, 2, 1, 0]:
+        enc.encode(clips[i], out=outs[i])
+        enc.sync()
+        assert torch.equal(outs[i], ref[i]), i
+    big = base.with_(batch=6)                        # grows the workspace: captured graphs are dropped
+    enc.encode(torch.from_numpy(synth.clip_u8(big)).cuda())
+    for i in [0, 1, 0, 1]:
+        enc.encode(clips[i], out=outs[i])
+        enc.sync()
+        assert torch.equal(outs[i], ref[i]), ("after growth", i)
+    new = torch.from_numpy(synth.clip_u8(base, first_clip=50)).cuda()
+    enc.set_graphs(False)
+    ref_new = enc.encode(new)["out"].clone()
+    enc.set_graphs(True)
+    clips[0].copy_(new)                               # same buffer, new contents, replayed graph
+    enc.encode(clips[0], out=outs[0])
+    enc.sync()
+    assert torch.equal(outs[0], ref_new)
+    enc.close()

@@ -231,6 +231,10 @@ class Encoder:
     def sync(self, stream=None):
         check(self.lib.jepa_encoder_sync(self.handle, _stream(stream)))
 
+    def set_graphs(self, on: bool):
+        """Replay of repeated encode calls as one CUDA graph (on by default)."""
+        check(self.lib.jepa_encoder_set_graphs(self.handle, int(bool(on))))
+
     def set_profiling(self, on: bool):
         check(self.lib.jepa_encoder_set_profiling(self.handle, int(on)))
 

@@ -550,6 +550,19 @@ struct jepa_encoder {
   size_t h_out_cap = 0;
   float* h_pool_dev = nullptr;
   size_t h_pool_cap = 0;
+  // Replay of repeated calls: one captured CUDA graph per call signature.
+  struct GraphEntry {
+    uint64_t key[10];
+    int eager_runs = 0;
+    cudaGraphExec_t exec = nullptr;
+    const void* ws = nullptr;     // the workspace and RoPE tables the graph was captured with
+    const void* rope = nullptr;
+    uint64_t last_use = 0;
+  };
+  std::vector<GraphEntry> graphs;
+  uint64_t calls = 0;
+  bool use_graphs = true;
+  cudaStream_t cap_stream = nullptr;
 };
 
 namespace {
@@ -722,6 +735,9 @@ void jepa_encoder_destroy(jepa_encoder* enc) {
   cudaFree(enc->h_clip_dev);
   cudaFree(enc->h_out_dev);
   cudaFree(enc->h_pool_dev);
+  for (auto& ge : enc->graphs)
+    if (ge.exec) cudaGraphExecDestroy(ge.exec);
+  if (enc->cap_stream) cudaStreamDestroy(enc->cap_stream);
   delete enc;
 }
 
@@ -765,17 +781,14 @@ jepa_status jepa_encoder_blocks(jepa_encoder* enc, float* x, int batch, int n_fr
                     enc->d_status, enc->prof, s, enc->sms);
 }
 
-jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_format, int batch, int n_frames, int height,
-                        int width, float* out_tokens, float* out_pooled, float* out_hier, void* stream) {
-  Geom g;
-  JEPA_TRY(check_clip(enc, batch, n_frames, height, width, g));
-  if (clip == nullptr || out_tokens == nullptr) return fail(JEPA_ERR_ARG, "clip and out_tokens are required");
-  if (!aligned16(clip) || !aligned16(out_tokens) || !aligned16(out_pooled) || !aligned16(out_hier))
-    return fail(JEPA_ERR_ARG, "device buffers must be 16-byte aligned");
-  if (clip_format != JEPA_CLIP_U8_THWC && clip_format != JEPA_CLIP_F32_CTHW)
-    return fail(JEPA_ERR_ARG, "clip_format %d", clip_format);
-  cudaStream_t s = (cudaStream_t)stream;
-  CUDA_TRY(cudaSetDevice(enc->device));
+}  // extern "C"
+
+namespace {
+
+// The device work of one jepa_encode call, enqueued on s (arguments checked).
+jepa_status encode_body(jepa_encoder* enc, const void* clip, int clip_format, int batch, int n_frames, int height,
+                        int width, const Geom& g, float* out_tokens, float* out_pooled, float* out_hier,
+                        cudaStream_t s) {
   JEPA_TRY(ensure_ws(enc, batch, g));
   const int hd = enc->p.embed_dim / enc->p.n_head;
   JEPA_TRY(rope_prepare(enc->rope, hd, enc->p.rope_layout, enc->p.rope_theta, g.gt, g.gh, g.gw,
@@ -794,6 +807,100 @@ jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_format, in
     Scope sc(enc->prof, P_OTHER, s);
     JEPA_TRY(cuda_status(mean_pool(out_tokens, out_pooled, batch, g.n_tok, D, s), "mean pool"));
   }
+  return JEPA_OK;
+}
+
+// Repeated calls with the same signature replay one CUDA graph: the first
+// runs eagerly (it sizes the workspace and builds the RoPE tables), the second
+// is captured on a private stream (the caller's may be the legacy default
+// stream, which cannot be captured) and every later one is a single graph
+// launch on the caller's stream.  A graph is dropped when the workspace or
+// the table buffer it points at has been reallocated.
+jepa_status encode_replayed(jepa_encoder* enc, const uint64_t (&key)[10], const void* clip, int clip_format,
+                            int batch, int n_frames, int height, int width, const Geom& g, float* out_tokens,
+                            float* out_pooled, float* out_hier, cudaStream_t s) {
+  using GE = jepa_encoder::GraphEntry;
+  GE* e = nullptr;
+  for (auto& x : enc->graphs)
+    if (memcmp(x.key, key, sizeof(key)) == 0) e = &x;
+  if (e == nullptr) {
+    if (enc->graphs.size() >= 8) {  // evict the least recently used signature
+      auto lru = enc->graphs.begin();
+      for (auto it = enc->graphs.begin(); it != enc->graphs.end(); ++it)
+        if (it->last_use < lru->last_use) lru = it;
+      if (lru->exec) cudaGraphExecDestroy(lru->exec);
+      enc->graphs.erase(lru);
+    }
+    enc->graphs.push_back(GE{});
+    e = &enc->graphs.back();
+    memcpy(e->key, key, sizeof(key));
+  }
+  e->last_use = ++enc->calls;
+  // workspace and tables for this signature, outside any capture
+  JEPA_TRY(ensure_ws(enc, batch, g));
+  const int hd = enc->p.embed_dim / enc->p.n_head;
+  JEPA_TRY(rope_prepare(enc->rope, hd, enc->p.rope_layout, enc->p.rope_theta, g.gt, g.gh, g.gw,
+                        enc->p.rope_interpolate, enc->p.rope_ref_grid, s));
+  if (e->exec != nullptr && (e->ws != enc->ws || e->rope != enc->rope.d)) {
+    cudaGraphExecDestroy(e->exec);
+    e->exec = nullptr;
+  }
+  if (e->exec == nullptr) {
+    if (e->eager_runs++ == 0)
+      return encode_body(enc, clip, clip_format, batch, n_frames, height, width, g, out_tokens, out_pooled, out_hier,
+                         s);
+    if (enc->cap_stream == nullptr) CUDA_TRY(cudaStreamCreateWithFlags(&enc->cap_stream, cudaStreamNonBlocking));
+    CUDA_TRY(cudaStreamBeginCapture(enc->cap_stream, cudaStreamCaptureModeThreadLocal));
+    const jepa_status st = encode_body(enc, clip, clip_format, batch, n_frames, height, width, g, out_tokens,
+                                       out_pooled, out_hier, enc->cap_stream);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(enc->cap_stream, &graph);
+    if (st != JEPA_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return st;
+    }
+    if (ce != cudaSuccess) return fail(JEPA_ERR_CUDA, "graph capture: %s", cudaGetErrorString(ce));
+    const cudaError_t ie = cudaGraphInstantiate(&e->exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ie != cudaSuccess) {
+      e->exec = nullptr;
+      return fail(JEPA_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(ie));
+    }
+    e->ws = enc->ws;
+    e->rope = enc->rope.d;
+  }
+  CUDA_TRY(cudaGraphLaunch(e->exec, s));
+  return JEPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_format, int batch, int n_frames, int height,
+                        int width, float* out_tokens, float* out_pooled, float* out_hier, void* stream) {
+  Geom g;
+  JEPA_TRY(check_clip(enc, batch, n_frames, height, width, g));
+  if (clip == nullptr || out_tokens == nullptr) return fail(JEPA_ERR_ARG, "clip and out_tokens are required");
+  if (!aligned16(clip) || !aligned16(out_tokens) || !aligned16(out_pooled) || !aligned16(out_hier))
+    return fail(JEPA_ERR_ARG, "device buffers must be 16-byte aligned");
+  if (clip_format != JEPA_CLIP_U8_THWC && clip_format != JEPA_CLIP_F32_CTHW)
+    return fail(JEPA_ERR_ARG, "clip_format %d", clip_format);
+  cudaStream_t s = (cudaStream_t)stream;
+  CUDA_TRY(cudaSetDevice(enc->device));
+  if (enc->prof.on || !enc->use_graphs)  // per-class events need the launches one by one
+    return encode_body(enc, clip, clip_format, batch, n_frames, height, width, g, out_tokens, out_pooled, out_hier,
+                       s);
+  const uint64_t key[10] = {(uint64_t)(uintptr_t)clip, (uint64_t)clip_format, (uint64_t)batch, (uint64_t)n_frames,
+                            (uint64_t)height, (uint64_t)width, (uint64_t)(uintptr_t)out_tokens,
+                            (uint64_t)(uintptr_t)out_pooled, (uint64_t)(uintptr_t)out_hier, 0};
+  return encode_replayed(enc, key, clip, clip_format, batch, n_frames, height, width, g, out_tokens, out_pooled,
+                         out_hier, s);
+}
+
+jepa_status jepa_encoder_set_graphs(jepa_encoder* enc, int on) {
+  if (enc == nullptr) return fail(JEPA_ERR_ARG, "encoder handle is NULL");
+  enc->use_graphs = on != 0;
   return JEPA_OK;
 }
 
