@@ -293,7 +293,7 @@ def main():
                                           for b in range(B)]).astype(np.int32)).cuda()
 
         def step():
-            return enc.encode_masked(clip, keep)["out"]
+            return enc.encode_masked(clip, keep, out=out)["out"]
 
     for _ in range(args.warmup):
         step()

@@ -158,8 +158,9 @@ JEPA_API jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_f
                         int height, int width, float* out_tokens, float* out_pooled, float* out_hier,
                         void* stream);
 
-/* jepa_encoder_set_graphs: replay of repeated jepa_encode calls (on by
- * default).  A call whose shapes and buffers equal an earlier call's runs as
+/* jepa_encoder_set_graphs: replay of repeated jepa_encode and
+ * jepa_encode_masked calls (on by default).  A call whose shapes and buffers
+ * (and, masked, id buffer and count) equal an earlier call's runs as
  * one CUDA graph launch on `stream`: the first such call runs eagerly, the
  * second is captured (on a stream private to the handle) and later ones
  * replay it, so the host issues one launch instead of one per kernel and the

@@ -275,3 +275,24 @@ def test_graph_replay_matches_eager(jg):
     enc.sync()
     assert torch.equal(outs[0], ref_new)
     enc.close()
+
+
+def test_masked_graph_replay_reads_current_ids(jg):
+    """A replayed masked call reads the current contents of its id buffer."""
+    cfg = SMALL["v2-hd32"]
+    w = synth.encoder_weights(cfg)
+    clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
+    k1, k2 = _keep(cfg, cfg.batch, 0.5, 8), _keep(cfg, cfg.batch, 0.5, 9)
+    enc = jg.Encoder(cfg, w)
+    enc.set_graphs(False)
+    ref1 = enc.encode_masked(clip, torch.from_numpy(k1).cuda())["out"].clone()
+    ref2 = enc.encode_masked(clip, torch.from_numpy(k2).cuda())["out"].clone()
+    enc.set_graphs(True)
+    ids = torch.from_numpy(k1).cuda()
+    got = torch.empty_like(ref1)
+    for want, src in [(ref1, k1), (ref1, k1), (ref1, k1), (ref2, k2), (ref1, k1)]:
+        ids.copy_(torch.from_numpy(src))
+        enc.encode_masked(clip, ids, out=got)   # same buffers every time: eager, capture, replays
+        enc.sync()
+        assert torch.equal(got, want)
+    enc.close()

@@ -190,14 +190,14 @@ class Encoder:
         return res
 
     def encode_masked(self, clip: torch.Tensor, ids_keep: torch.Tensor, pooled: bool = False, hier: bool = False,
-                      stream=None):
+                      stream=None, out=None):
         """Masked encoder forward: only the tokens ids_keep [B, K] (int32,
         device) of each clip go through the blocks, at their true positions."""
         fmt = _lib.CLIP_U8_THWC if clip.dtype == torch.uint8 else _lib.CLIP_F32_CTHW
         B, T, H, W = (clip.shape[:4] if fmt == _lib.CLIP_U8_THWC else (clip.shape[0],) + tuple(clip.shape[2:5]))
         K, D = ids_keep.shape[1], self.cfg.embed_dim
         dev = clip.device
-        out = torch.empty((B, K, D), dtype=torch.float32, device=dev)
+        out = out if out is not None else torch.empty((B, K, D), dtype=torch.float32, device=dev)
         pool = torch.empty((B, D), dtype=torch.float32, device=dev) if pooled else None
         nh = len(self.cfg.hier_layers)
         taps = torch.empty((nh, B, K, D), dtype=torch.float32, device=dev) if (hier and nh) else None

@@ -552,7 +552,7 @@ struct jepa_encoder {
   size_t h_pool_cap = 0;
   // Replay of repeated calls: one captured CUDA graph per call signature.
   struct GraphEntry {
-    uint64_t key[10];
+    uint64_t key[12];
     int eager_runs = 0;
     cudaGraphExec_t exec = nullptr;
     const void* ws = nullptr;     // the workspace and RoPE tables the graph was captured with
@@ -816,9 +816,11 @@ jepa_status encode_body(jepa_encoder* enc, const void* clip, int clip_format, in
 // stream, which cannot be captured) and every later one is a single graph
 // launch on the caller's stream.  A graph is dropped when the workspace or
 // the table buffer it points at has been reallocated.
-jepa_status encode_replayed(jepa_encoder* enc, const uint64_t (&key)[10], const void* clip, int clip_format,
-                            int batch, int n_frames, int height, int width, const Geom& g, float* out_tokens,
-                            float* out_pooled, float* out_hier, cudaStream_t s) {
+// `body(stream)` enqueues the call's device work; `gw` is the geometry the
+// workspace is sized for and `g` the grid of the RoPE tables.
+template <typename Body>
+jepa_status encode_replayed(jepa_encoder* enc, const uint64_t (&key)[12], int batch, const Geom& gw, const Geom& g,
+                            Body&& body, cudaStream_t s) {
   using GE = jepa_encoder::GraphEntry;
   GE* e = nullptr;
   for (auto& x : enc->graphs)
@@ -837,7 +839,7 @@ jepa_status encode_replayed(jepa_encoder* enc, const uint64_t (&key)[10], const 
   }
   e->last_use = ++enc->calls;
   // workspace and tables for this signature, outside any capture
-  JEPA_TRY(ensure_ws(enc, batch, g));
+  JEPA_TRY(ensure_ws(enc, batch, gw));
   const int hd = enc->p.embed_dim / enc->p.n_head;
   JEPA_TRY(rope_prepare(enc->rope, hd, enc->p.rope_layout, enc->p.rope_theta, g.gt, g.gh, g.gw,
                         enc->p.rope_interpolate, enc->p.rope_ref_grid, s));
@@ -846,13 +848,10 @@ jepa_status encode_replayed(jepa_encoder* enc, const uint64_t (&key)[10], const 
     e->exec = nullptr;
   }
   if (e->exec == nullptr) {
-    if (e->eager_runs++ == 0)
-      return encode_body(enc, clip, clip_format, batch, n_frames, height, width, g, out_tokens, out_pooled, out_hier,
-                         s);
+    if (e->eager_runs++ == 0) return body(s);
     if (enc->cap_stream == nullptr) CUDA_TRY(cudaStreamCreateWithFlags(&enc->cap_stream, cudaStreamNonBlocking));
     CUDA_TRY(cudaStreamBeginCapture(enc->cap_stream, cudaStreamCaptureModeThreadLocal));
-    const jepa_status st = encode_body(enc, clip, clip_format, batch, n_frames, height, width, g, out_tokens,
-                                       out_pooled, out_hier, enc->cap_stream);
+    const jepa_status st = body(enc->cap_stream);
     cudaGraph_t graph = nullptr;
     const cudaError_t ce = cudaStreamEndCapture(enc->cap_stream, &graph);
     if (st != JEPA_OK) {
@@ -891,11 +890,12 @@ jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_format, in
   if (enc->prof.on || !enc->use_graphs)  // per-class events need the launches one by one
     return encode_body(enc, clip, clip_format, batch, n_frames, height, width, g, out_tokens, out_pooled, out_hier,
                        s);
-  const uint64_t key[10] = {(uint64_t)(uintptr_t)clip, (uint64_t)clip_format, (uint64_t)batch, (uint64_t)n_frames,
-                            (uint64_t)height, (uint64_t)width, (uint64_t)(uintptr_t)out_tokens,
-                            (uint64_t)(uintptr_t)out_pooled, (uint64_t)(uintptr_t)out_hier, 0};
-  return encode_replayed(enc, key, clip, clip_format, batch, n_frames, height, width, g, out_tokens, out_pooled,
-                         out_hier, s);
+  const uint64_t key[12] = {1, (uint64_t)(uintptr_t)clip, (uint64_t)clip_format, (uint64_t)batch,
+                            (uint64_t)n_frames, (uint64_t)height, (uint64_t)width, (uint64_t)(uintptr_t)out_tokens,
+                            (uint64_t)(uintptr_t)out_pooled, (uint64_t)(uintptr_t)out_hier, 0, 0};
+  return encode_replayed(enc, key, batch, g, g, [&](cudaStream_t st) {
+    return encode_body(enc, clip, clip_format, batch, n_frames, height, width, g, out_tokens, out_pooled, out_hier, st);
+  }, s);
 }
 
 jepa_status jepa_encoder_set_graphs(jepa_encoder* enc, int on) {
@@ -920,27 +920,36 @@ jepa_status jepa_encode_masked(jepa_encoder* enc, const void* clip, int clip_for
   CUDA_TRY(cudaSetDevice(enc->device));
   Geom gk = g;  // the blocks see n_keep tokens per clip
   gk.n_tok = n_keep;
-  JEPA_TRY(ensure_ws(enc, batch, gk));
-  const int hd = enc->p.embed_dim / enc->p.n_head;
-  // RoPE tables for the full grid: each kept token keeps its own grid cell
-  JEPA_TRY(rope_prepare(enc->rope, hd, enc->p.rope_layout, enc->p.rope_theta, g.gt, g.gh, g.gw,
-                        enc->p.rope_interpolate, enc->p.rope_ref_grid, s));
-  Work w = carve(enc->ws, enc->p.dtype, batch, n_keep, enc->p.embed_dim, enc->p.ffn_dim, 1536, false);
-  JEPA_TRY(cuda_status(check_ids(ids_keep, (long)batch * n_keep, g.n_tok, enc->d_status, s), "id check"));
-  JEPA_TRY(embed_into(enc, w, clip, clip_format, batch, n_frames, height, width, g, w.x, s, ids_keep, n_keep));
-  JEPA_TRY(run_blocks(enc_stack(enc), w, batch, n_keep, 0, enc->p.n_layer, enc->rope.rp, ids_keep, out_hier,
-                      enc->d_status, enc->prof, s, enc->sms));
-  const int M = batch * n_keep, D = enc->p.embed_dim;
-  {
-    Scope sc(enc->prof, P_LN, s);
-    JEPA_TRY(cuda_status(layernorm(DTYPE_F32, w.x, enc->norm_w, enc->norm_b, out_tokens, M, D, enc->p.ln_eps, s),
-                         "final layernorm"));
-  }
-  if (out_pooled != nullptr) {
-    Scope sc(enc->prof, P_OTHER, s);
-    JEPA_TRY(cuda_status(mean_pool(out_tokens, out_pooled, batch, n_keep, D, s), "mean pool"));
-  }
-  return JEPA_OK;
+  auto body = [&](cudaStream_t st) -> jepa_status {
+    JEPA_TRY(ensure_ws(enc, batch, gk));
+    const int hd = enc->p.embed_dim / enc->p.n_head;
+    // RoPE tables for the full grid: each kept token keeps its own grid cell
+    JEPA_TRY(rope_prepare(enc->rope, hd, enc->p.rope_layout, enc->p.rope_theta, g.gt, g.gh, g.gw,
+                          enc->p.rope_interpolate, enc->p.rope_ref_grid, st));
+    Work w = carve(enc->ws, enc->p.dtype, batch, n_keep, enc->p.embed_dim, enc->p.ffn_dim, 1536, false);
+    JEPA_TRY(cuda_status(check_ids(ids_keep, (long)batch * n_keep, g.n_tok, enc->d_status, st), "id check"));
+    JEPA_TRY(embed_into(enc, w, clip, clip_format, batch, n_frames, height, width, g, w.x, st, ids_keep, n_keep));
+    JEPA_TRY(run_blocks(enc_stack(enc), w, batch, n_keep, 0, enc->p.n_layer, enc->rope.rp, ids_keep, out_hier,
+                        enc->d_status, enc->prof, st, enc->sms));
+    const int M = batch * n_keep, D = enc->p.embed_dim;
+    {
+      Scope sc(enc->prof, P_LN, st);
+      JEPA_TRY(cuda_status(layernorm(DTYPE_F32, w.x, enc->norm_w, enc->norm_b, out_tokens, M, D, enc->p.ln_eps, st),
+                           "final layernorm"));
+    }
+    if (out_pooled != nullptr) {
+      Scope sc(enc->prof, P_OTHER, st);
+      JEPA_TRY(cuda_status(mean_pool(out_tokens, out_pooled, batch, n_keep, D, st), "mean pool"));
+    }
+    return JEPA_OK;
+  };
+  if (enc->prof.on || !enc->use_graphs) return body(s);
+  // the ids are read at run time: a replay sees their current contents
+  const uint64_t key[12] = {2, (uint64_t)(uintptr_t)clip, (uint64_t)clip_format, (uint64_t)batch,
+                            (uint64_t)n_frames, (uint64_t)height, (uint64_t)width, (uint64_t)(uintptr_t)out_tokens,
+                            (uint64_t)(uintptr_t)out_pooled, (uint64_t)(uintptr_t)out_hier,
+                            (uint64_t)(uintptr_t)ids_keep, (uint64_t)n_keep};
+  return encode_replayed(enc, key, batch, gk, g, body, s);
 }
 
 jepa_status jepa_encode_host(jepa_encoder* enc, const void* host_clip, int clip_format, int batch, int n_frames,
