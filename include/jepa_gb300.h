@@ -237,6 +237,10 @@ JEPA_API jepa_status jepa_predict_ex(jepa_predictor* pred, const float* enc_toke
                                      int grid_t, int grid_h, int grid_w, int modality, float* out, float* out_ctx,
                                      void* stream);
 JEPA_API jepa_status jepa_predictor_sync(jepa_predictor* pred, void* stream);
+/* Replay of repeated jepa_predict / jepa_predict_ex calls as one CUDA graph,
+ * as jepa_encoder_set_graphs (on by default; the id buffers are read at run
+ * time, so a replay sees their current contents). */
+JEPA_API jepa_status jepa_predictor_set_graphs(jepa_predictor* pred, int on);
 
 /* ---------------------------------------------------------------- single operations
  * The kernels of the encoder, callable one at a time (the same code runs

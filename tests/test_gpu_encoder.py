@@ -296,3 +296,36 @@ def test_masked_graph_replay_reads_current_ids(jg):
         enc.sync()
         assert torch.equal(got, want)
     enc.close()
+
+
+def test_predictor_graph_replay(jg):
+    """Replayed predictor calls equal eager ones and read the current ids."""
+    import dataclasses
+    pc = dataclasses.replace(synth.PREDICTOR_21, n_layer=2)
+    cfg = synth.CONFIGS["pred21"].with_(n_frames=4, height=96, width=80, predictor=pc)
+    pw = synth.predictor_weights(cfg)
+    grid = cfg.grid()
+    n = grid[0] * grid[1] * grid[2]
+    enc = torch.from_numpy(synth.round_to_dtype(np.random.default_rng(2).standard_normal((n, 768)), "f32")).cuda()
+    splits = []
+    for seed in (0, 1):
+        perm = np.random.default_rng(seed).permutation(n).astype(np.int32)
+        splits.append((np.sort(perm[: n // 2]), np.sort(perm[n // 2:])))
+    pred = jg.Predictor(pc, pw, cfg.dtype)
+    pred.set_graphs(False)
+    refs = []
+    for c, t in splits:
+        o, oc = pred.predict(enc, torch.from_numpy(c).cuda(), torch.from_numpy(t).cuda(), grid, modality="video",
+                             with_ctx=True)
+        refs.append((o.clone(), oc.clone()))
+    pred.set_graphs(True)
+    ic = torch.from_numpy(splits[0][0]).cuda()
+    it = torch.from_numpy(splits[0][1]).cuda()
+    out, octx = torch.empty_like(refs[0][0]), torch.empty_like(refs[0][1])
+    for k in (0, 0, 0, 1, 0, 1):
+        ic.copy_(torch.from_numpy(splits[k][0]))
+        it.copy_(torch.from_numpy(splits[k][1]))
+        pred.predict(enc, ic, it, grid, modality="video", with_ctx=True, out=out, out_ctx=octx)
+        pred.sync()
+        assert torch.equal(out, refs[k][0]) and torch.equal(octx, refs[k][1]), k
+    pred.close()

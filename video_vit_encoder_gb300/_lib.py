@@ -66,6 +66,7 @@ SIGNATURES = {
     "jepa_predict": (ST, [VP, VP, I, VP, I, VP, I, I, I, I, VP, VP]),
     "jepa_encode_masked": (ST, [VP, VP, I, I, I, I, I, VP, I, VP, VP, VP, VP]),
     "jepa_encoder_set_graphs": (ST, [VP, I]),
+    "jepa_predictor_set_graphs": (ST, [VP, I]),
     "jepa_predict_ex": (ST, [VP, VP, I, VP, I, VP, I, I, I, I, I, VP, VP, VP]),
     "jepa_predictor_sync": (ST, [VP, VP]),
     "jepa_layernorm_f32": (ST, [VP, VP, VP, VP, I, I, F, VP]),

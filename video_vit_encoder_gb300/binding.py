@@ -274,12 +274,17 @@ class Predictor:
         except Exception:
             pass
 
+    def set_graphs(self, on: bool):
+        """Replay of repeated predict calls as one CUDA graph (on by default)."""
+        check(self.lib.jepa_predictor_set_graphs(self.handle, int(bool(on))))
+
     def predict(self, enc_tokens: torch.Tensor, ids_ctx: torch.Tensor, ids_tgt: torch.Tensor, grid, stream=None,
-                modality: str | None = None, with_ctx: bool = False):
+                modality: str | None = None, with_ctx: bool = False, out=None, out_ctx=None):
         """Target predictions [n_tgt, out_dim]; with ``with_ctx`` also the
         context projection [n_ctx, out_dim] (2.1), as ``(pred, ctx)``.
         modality: None (the plain call: video), "video", "image" or "auto"."""
-        out = torch.empty((ids_tgt.numel(), self.pcfg.out_dim), dtype=torch.float32, device=enc_tokens.device)
+        out = out if out is not None else torch.empty((ids_tgt.numel(), self.pcfg.out_dim), dtype=torch.float32,
+                                                      device=enc_tokens.device)
         gt, gh, gw = grid
         if modality is None and not with_ctx:
             check(self.lib.jepa_predict(self.handle, _ptr(enc_tokens), enc_tokens.shape[0], _ptr(ids_ctx),
@@ -288,8 +293,9 @@ class Predictor:
             return out
         mod = {None: _lib.MODALITY_VIDEO, "video": _lib.MODALITY_VIDEO, "image": _lib.MODALITY_IMAGE,
                "auto": _lib.MODALITY_AUTO}[modality]
-        ctx = (torch.empty((ids_ctx.numel(), self.pcfg.out_dim), dtype=torch.float32, device=enc_tokens.device)
-               if with_ctx else None)
+        ctx = (out_ctx if out_ctx is not None else
+               torch.empty((ids_ctx.numel(), self.pcfg.out_dim), dtype=torch.float32, device=enc_tokens.device)
+               ) if with_ctx else None
         check(self.lib.jepa_predict_ex(self.handle, _ptr(enc_tokens), enc_tokens.shape[0], _ptr(ids_ctx),
                                        ids_ctx.numel(), _ptr(ids_tgt), ids_tgt.numel(), gt, gh, gw, mod, _ptr(out),
                                        _ptr(ctx), _stream(stream)))

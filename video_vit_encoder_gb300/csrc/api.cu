@@ -213,6 +213,30 @@ struct RopeCache {
   RopeParams rp{};
 };
 
+// Replay of repeated calls: one captured CUDA graph per call signature (the
+// 8 most recently used), with the workspace and table buffers it points at.
+struct GraphCache {
+  struct Entry {
+    uint64_t key[12];
+    int eager_runs = 0;
+    cudaGraphExec_t exec = nullptr;
+    const void* ws = nullptr;
+    const void* rope = nullptr;
+    uint64_t last_use = 0;
+  };
+  std::vector<Entry> entries;
+  uint64_t calls = 0;
+  bool on = true;
+  cudaStream_t cap = nullptr;  // capture stream, private to the owning handle
+  void release() {
+    for (auto& e : entries)
+      if (e.exec) cudaGraphExecDestroy(e.exec);
+    entries.clear();
+    if (cap) cudaStreamDestroy(cap);
+    cap = nullptr;
+  }
+};
+
 // Builds the per-axis cos/sin tables for a grid ("V-JEPA 2 / 2.1 ...", §4:
 // omega_k = theta^(-k/(d/2)); §4.3: interpolated spatial positions
 // p*(ref-1)/(n-1), evaluated left to right) in double and uploads them.
@@ -550,19 +574,7 @@ struct jepa_encoder {
   size_t h_out_cap = 0;
   float* h_pool_dev = nullptr;
   size_t h_pool_cap = 0;
-  // Replay of repeated calls: one captured CUDA graph per call signature.
-  struct GraphEntry {
-    uint64_t key[12];
-    int eager_runs = 0;
-    cudaGraphExec_t exec = nullptr;
-    const void* ws = nullptr;     // the workspace and RoPE tables the graph was captured with
-    const void* rope = nullptr;
-    uint64_t last_use = 0;
-  };
-  std::vector<GraphEntry> graphs;
-  uint64_t calls = 0;
-  bool use_graphs = true;
-  cudaStream_t cap_stream = nullptr;
+  GraphCache graphs;
 };
 
 namespace {
@@ -735,9 +747,7 @@ void jepa_encoder_destroy(jepa_encoder* enc) {
   cudaFree(enc->h_clip_dev);
   cudaFree(enc->h_out_dev);
   cudaFree(enc->h_pool_dev);
-  for (auto& ge : enc->graphs)
-    if (ge.exec) cudaGraphExecDestroy(ge.exec);
-  if (enc->cap_stream) cudaStreamDestroy(enc->cap_stream);
+  enc->graphs.release();
   delete enc;
 }
 
@@ -816,44 +826,41 @@ jepa_status encode_body(jepa_encoder* enc, const void* clip, int clip_format, in
 // stream, which cannot be captured) and every later one is a single graph
 // launch on the caller's stream.  A graph is dropped when the workspace or
 // the table buffer it points at has been reallocated.
-// `body(stream)` enqueues the call's device work; `gw` is the geometry the
-// workspace is sized for and `g` the grid of the RoPE tables.
-template <typename Body>
-jepa_status encode_replayed(jepa_encoder* enc, const uint64_t (&key)[12], int batch, const Geom& gw, const Geom& g,
-                            Body&& body, cudaStream_t s) {
-  using GE = jepa_encoder::GraphEntry;
-  GE* e = nullptr;
-  for (auto& x : enc->graphs)
+// `prep(stream)` readies the workspace and tables outside any capture;
+// `ws` and `rope` are the owner's buffer pointers (read after prep);
+// `body(stream)` enqueues the call's device work.
+template <typename Prep, typename Body>
+jepa_status replay(GraphCache& gc, const uint64_t (&key)[12], Prep&& prep, void* const& ws, float* const& rope,
+                   Body&& body, cudaStream_t s) {
+  using E = GraphCache::Entry;
+  E* e = nullptr;
+  for (auto& x : gc.entries)
     if (memcmp(x.key, key, sizeof(key)) == 0) e = &x;
   if (e == nullptr) {
-    if (enc->graphs.size() >= 8) {  // evict the least recently used signature
-      auto lru = enc->graphs.begin();
-      for (auto it = enc->graphs.begin(); it != enc->graphs.end(); ++it)
+    if (gc.entries.size() >= 8) {  // evict the least recently used signature
+      auto lru = gc.entries.begin();
+      for (auto it = gc.entries.begin(); it != gc.entries.end(); ++it)
         if (it->last_use < lru->last_use) lru = it;
       if (lru->exec) cudaGraphExecDestroy(lru->exec);
-      enc->graphs.erase(lru);
+      gc.entries.erase(lru);
     }
-    enc->graphs.push_back(GE{});
-    e = &enc->graphs.back();
+    gc.entries.push_back(E{});
+    e = &gc.entries.back();
     memcpy(e->key, key, sizeof(key));
   }
-  e->last_use = ++enc->calls;
-  // workspace and tables for this signature, outside any capture
-  JEPA_TRY(ensure_ws(enc, batch, gw));
-  const int hd = enc->p.embed_dim / enc->p.n_head;
-  JEPA_TRY(rope_prepare(enc->rope, hd, enc->p.rope_layout, enc->p.rope_theta, g.gt, g.gh, g.gw,
-                        enc->p.rope_interpolate, enc->p.rope_ref_grid, s));
-  if (e->exec != nullptr && (e->ws != enc->ws || e->rope != enc->rope.d)) {
+  e->last_use = ++gc.calls;
+  JEPA_TRY(prep(s));
+  if (e->exec != nullptr && (e->ws != ws || e->rope != rope)) {
     cudaGraphExecDestroy(e->exec);
     e->exec = nullptr;
   }
   if (e->exec == nullptr) {
     if (e->eager_runs++ == 0) return body(s);
-    if (enc->cap_stream == nullptr) CUDA_TRY(cudaStreamCreateWithFlags(&enc->cap_stream, cudaStreamNonBlocking));
-    CUDA_TRY(cudaStreamBeginCapture(enc->cap_stream, cudaStreamCaptureModeThreadLocal));
-    const jepa_status st = body(enc->cap_stream);
+    if (gc.cap == nullptr) CUDA_TRY(cudaStreamCreateWithFlags(&gc.cap, cudaStreamNonBlocking));
+    CUDA_TRY(cudaStreamBeginCapture(gc.cap, cudaStreamCaptureModeThreadLocal));
+    const jepa_status st = body(gc.cap);
     cudaGraph_t graph = nullptr;
-    const cudaError_t ce = cudaStreamEndCapture(enc->cap_stream, &graph);
+    const cudaError_t ce = cudaStreamEndCapture(gc.cap, &graph);
     if (st != JEPA_OK) {
       if (graph) cudaGraphDestroy(graph);
       return st;
@@ -865,11 +872,24 @@ jepa_status encode_replayed(jepa_encoder* enc, const uint64_t (&key)[12], int ba
       e->exec = nullptr;
       return fail(JEPA_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(ie));
     }
-    e->ws = enc->ws;
-    e->rope = enc->rope.d;
+    e->ws = ws;
+    e->rope = rope;
   }
   CUDA_TRY(cudaGraphLaunch(e->exec, s));
   return JEPA_OK;
+}
+
+// The encoder's replay: workspace for geometry gw, RoPE tables for grid g.
+template <typename Body>
+jepa_status encode_replayed(jepa_encoder* enc, const uint64_t (&key)[12], int batch, const Geom& gw, const Geom& g,
+                            Body&& body, cudaStream_t s) {
+  auto prep = [&](cudaStream_t st) -> jepa_status {
+    JEPA_TRY(ensure_ws(enc, batch, gw));
+    const int hd = enc->p.embed_dim / enc->p.n_head;
+    return rope_prepare(enc->rope, hd, enc->p.rope_layout, enc->p.rope_theta, g.gt, g.gh, g.gw,
+                        enc->p.rope_interpolate, enc->p.rope_ref_grid, st);
+  };
+  return replay(enc->graphs, key, prep, enc->ws, enc->rope.d, body, s);
 }
 
 }  // namespace
@@ -887,7 +907,7 @@ jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_format, in
     return fail(JEPA_ERR_ARG, "clip_format %d", clip_format);
   cudaStream_t s = (cudaStream_t)stream;
   CUDA_TRY(cudaSetDevice(enc->device));
-  if (enc->prof.on || !enc->use_graphs)  // per-class events need the launches one by one
+  if (enc->prof.on || !enc->graphs.on)  // per-class events need the launches one by one
     return encode_body(enc, clip, clip_format, batch, n_frames, height, width, g, out_tokens, out_pooled, out_hier,
                        s);
   const uint64_t key[12] = {1, (uint64_t)(uintptr_t)clip, (uint64_t)clip_format, (uint64_t)batch,
@@ -900,7 +920,7 @@ jepa_status jepa_encode(jepa_encoder* enc, const void* clip, int clip_format, in
 
 jepa_status jepa_encoder_set_graphs(jepa_encoder* enc, int on) {
   if (enc == nullptr) return fail(JEPA_ERR_ARG, "encoder handle is NULL");
-  enc->use_graphs = on != 0;
+  enc->graphs.on = on != 0;
   return JEPA_OK;
 }
 
@@ -943,7 +963,7 @@ jepa_status jepa_encode_masked(jepa_encoder* enc, const void* clip, int clip_for
     }
     return JEPA_OK;
   };
-  if (enc->prof.on || !enc->use_graphs) return body(s);
+  if (enc->prof.on || !enc->graphs.on) return body(s);
   // the ids are read at run time: a replay sees their current contents
   const uint64_t key[12] = {2, (uint64_t)(uintptr_t)clip, (uint64_t)clip_format, (uint64_t)batch,
                             (uint64_t)n_frames, (uint64_t)height, (uint64_t)width, (uint64_t)(uintptr_t)out_tokens,
@@ -1024,6 +1044,7 @@ jepa_status jepa_encoder_profile(jepa_encoder* enc, double* times_ms, long long*
 
 // ============================================================================= predictor
 struct jepa_predictor {
+  GraphCache graphs;
   jepa_predictor_params p{};
   int device = 0, sms = 0;
   void* d_weights = nullptr;
@@ -1125,6 +1146,7 @@ void jepa_predictor_destroy(jepa_predictor* pr) {
     cudaFree(pr->b_emb_mod[m]);
     cudaFree(pr->mask_mod[m]);
   }
+  pr->graphs.release();
   delete pr;
 }
 
@@ -1154,20 +1176,25 @@ jepa_status jepa_predict_ex(jepa_predictor* pr, const float* enc_tokens, int n_t
     return fail(JEPA_ERR_ARG, "grid %dx%dx%d does not hold %d tokens", grid_t, grid_h, grid_w, n_tokens);
   const int D = pr->p.embed_dim, F = pr->p.ffn_dim, n = n_ctx + n_tgt;
   if ((long long)n * std::max(F, 3 * D) >= (1ll << 31)) return fail(JEPA_ERR_ARG, "too many rows");
-  cudaStream_t s = (cudaStream_t)stream;
+  cudaStream_t s0 = (cudaStream_t)stream;
   CUDA_TRY(cudaSetDevice(pr->device));
   const int dt = pr->p.dtype;
-  const size_t need = work_bytes(dt, 1, n, D, F, pr->p.in_dim, true);
-  if (need > pr->ws_bytes) {
-    cudaFree(pr->ws);
-    pr->ws = nullptr;
-    pr->ws_bytes = 0;
-    if (cudaMalloc(&pr->ws, need) != cudaSuccess) return fail(JEPA_ERR_OOM, "predictor workspace");
-    if (cudaMemset(pr->ws, 0, need) != cudaSuccess) return fail(JEPA_ERR_CUDA, "predictor workspace memset");
-    pr->ws_bytes = need;
-  }
   const int hd = D / pr->p.n_head;
-  JEPA_TRY(rope_prepare(pr->rope, hd, pr->p.rope_layout, pr->p.rope_theta, grid_t, grid_h, grid_w, 0, 0, s));
+  // workspace and RoPE tables (no-ops once sized and built for this grid)
+  auto prep = [&](cudaStream_t s) -> jepa_status {
+    const size_t need = work_bytes(dt, 1, n, D, F, pr->p.in_dim, true);
+    if (need > pr->ws_bytes) {
+      cudaFree(pr->ws);
+      pr->ws = nullptr;
+      pr->ws_bytes = 0;
+      if (cudaMalloc(&pr->ws, need) != cudaSuccess) return fail(JEPA_ERR_OOM, "predictor workspace");
+      if (cudaMemset(pr->ws, 0, need) != cudaSuccess) return fail(JEPA_ERR_CUDA, "predictor workspace memset");
+      pr->ws_bytes = need;
+    }
+    return rope_prepare(pr->rope, hd, pr->p.rope_layout, pr->p.rope_theta, grid_t, grid_h, grid_w, 0, 0, s);
+  };
+  auto body = [&](cudaStream_t s) -> jepa_status {
+  JEPA_TRY(prep(s));
   Work w = carve(pr->ws, dt, 1, n, D, F, pr->p.in_dim, true);
   // positions of the concatenated sequence: context ids then target ids
   CUDA_TRY(cudaMemcpyAsync(w.pos, ids_ctx, sizeof(int) * n_ctx, cudaMemcpyDeviceToDevice, s));
@@ -1222,6 +1249,19 @@ jepa_status jepa_predict_ex(jepa_predictor* pr, const float* enc_tokens, int n_t
       JEPA_TRY(run_linear(dt, EPI_F32, w.y, pr->w_projc, n_ctx, pr->p.out_dim, D, ec, pr->d_status, s, pr->sms));
     }
   }
+  return JEPA_OK;
+  };
+  if (pr->prof.on || !pr->graphs.on) return body(s0);
+  const uint64_t key[12] = {3, (uint64_t)(uintptr_t)enc_tokens, (uint64_t)n_tokens | ((uint64_t)n_ctx << 32),
+                            (uint64_t)(uintptr_t)ids_ctx, (uint64_t)(uintptr_t)ids_tgt, (uint64_t)n_tgt,
+                            (uint64_t)grid_t | ((uint64_t)grid_h << 32), (uint64_t)grid_w, (uint64_t)mod,
+                            (uint64_t)(uintptr_t)out, (uint64_t)(uintptr_t)out_ctx, 0};
+  return replay(pr->graphs, key, prep, pr->ws, pr->rope.d, body, s0);
+}
+
+jepa_status jepa_predictor_set_graphs(jepa_predictor* pr, int on) {
+  if (pr == nullptr) return fail(JEPA_ERR_ARG, "predictor handle is NULL");
+  pr->graphs.on = on != 0;
   return JEPA_OK;
 }
 
