@@ -56,6 +56,15 @@ template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t u) {
 // Exact-erf GELU, 0.5 z (1 + erf(z / sqrt 2)).
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 
+// (a, b) += (x, y) as one packed f32x2 add.
+__device__ __forceinline__ void add2f(float& a, float& b, float x, float y) {
+  uint64_t p, q;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(q) : "f"(x), "f"(y));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(p) : "l"(q));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(p));
+}
+
 // GELU(z) = 0.5 z (1 + erf(z / sqrt 2)) for two values at once, with erf from
 // Abramowitz & Stegun, Handbook of Mathematical Functions, eq. 7.1.28
 // (Hastings): erf(x) = 1 - (1 + a1 x + ... + a6 x^6)^-16 for x >= 0, absolute
@@ -63,17 +72,12 @@ __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + e
 // reciprocal per value; for the 16-bit outputs of the tensor-core path (the
 // fp32 path keeps erff).
 __device__ __forceinline__ void gelu_as2(float& z0, float& z1) {
-  uint64_t z, u, p;
+  // u = z / sqrt(2) for both values; |u| by clearing both sign bits at once
+  uint64_t z, u, p, ax;
   asm("mov.b64 %0, {%1, %2};" : "=l"(z) : "f"(z0), "f"(z1));
   const float k = 0.70710678118654752f;
   asm("{\n\t.reg .b64 kk;\n\tmov.b64 kk, {%2, %2};\n\tmul.rn.f32x2 %0, %1, kk;\n\t}" : "=l"(u) : "l"(z), "f"(k));
-  // |x|
-  float ua, ub;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(ua), "=f"(ub) : "l"(u));
-  const float sa = ua, sb = ub;
-  ua = fabsf(ua);
-  ub = fabsf(ub);
-  asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(ua), "f"(ub));
+  asm("and.b64 %0, %1, 0x7FFFFFFF7FFFFFFF;" : "=l"(ax) : "l"(u));
 #define JEPA_C2(name, v) uint64_t name; asm("mov.b64 %0, {%1, %1};" : "=l"(name) : "f"(v));
   JEPA_C2(a6, 0.0000430638f)
   JEPA_C2(a5, 0.0002765672f)
@@ -82,26 +86,31 @@ __device__ __forceinline__ void gelu_as2(float& z0, float& z1) {
   JEPA_C2(a2, 0.0422820123f)
   JEPA_C2(a1, 0.0705230784f)
   JEPA_C2(one, 1.0f)
+  JEPA_C2(half, 0.5f)
 #undef JEPA_C2
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(p) : "l"(u), "l"(a6), "l"(a5));
-  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(u), "l"(a4));
-  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(u), "l"(a3));
-  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(u), "l"(a2));
-  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(u), "l"(a1));
-  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(u), "l"(one));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(p) : "l"(ax), "l"(a6), "l"(a5));
+  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(ax), "l"(a4));
+  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(ax), "l"(a3));
+  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(ax), "l"(a2));
+  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(ax), "l"(a1));
+  asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(p) : "l"(ax), "l"(one));
   asm("mul.rn.f32x2 %0, %0, %0;" : "+l"(p));  // ^2
   asm("mul.rn.f32x2 %0, %0, %0;" : "+l"(p));  // ^4
   asm("mul.rn.f32x2 %0, %0, %0;" : "+l"(p));  // ^8
   asm("mul.rn.f32x2 %0, %0, %0;" : "+l"(p));  // ^16
   float pa, pb;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(pa), "=f"(pb) : "l"(p));
-  float ra, rb;  // 1/p^16 (0 once p^16 overflows: erf = +-1 there)
+  float ra, rb;  // r = 1/p^16 = 1 - |erf(u)| (0 once p^16 overflows: erf = +-1 there)
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(ra) : "f"(pa));
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rb) : "f"(pb));
-  const float ea = copysignf(1.0f - ra, sa);
-  const float eb = copysignf(1.0f - rb, sb);
-  z0 = 0.5f * z0 * (1.0f + ea);
-  z1 = 0.5f * z1 * (1.0f + eb);
+  // gelu(z) = z/2 (1 + erf(u)) = z - z r / 2 for z >= 0, z r / 2 for z < 0
+  uint64_t r, h;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(ra), "f"(rb));
+  asm("{\n\t.reg .b64 zh;\n\tmul.rn.f32x2 zh, %1, %2;\n\tmul.rn.f32x2 %0, zh, %3;\n\t}" : "=l"(h) : "l"(z), "l"(half), "l"(r));
+  float ha, hb;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(ha), "=f"(hb) : "l"(h));
+  z0 = z0 >= 0.0f ? z0 - ha : ha;
+  z1 = z1 >= 0.0f ? z1 - hb : hb;
 }
 
 // ----------------------------------------------------------------------------- misc PTX

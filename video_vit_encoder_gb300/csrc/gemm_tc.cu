@@ -98,10 +98,8 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
         const float4 bb = __ldg(reinterpret_cast<const float4*>(b + i));
-        v[i] += bb.x;
-        v[i + 1] += bb.y;
-        v[i + 2] += bb.z;
-        v[i + 3] += bb.w;
+        add2f(v[i], v[i + 1], bb.x, bb.y);
+        add2f(v[i + 2], v[i + 3], bb.z, bb.w);
       }
     }
     const int d0 = (c * 32) % HD;
@@ -170,10 +168,8 @@ __device__ __forceinline__ void resid_epilogue(const EpiParams& ep, const CUtens
 #pragma unroll
       for (int i = 0; i < kCols / 4; ++i) {
         const float4 bb = __ldg(b4 + i);
-        v[4 * i] += bb.x;
-        v[4 * i + 1] += bb.y;
-        v[4 * i + 2] += bb.z;
-        v[4 * i + 3] += bb.w;
+        add2f(v[4 * i], v[4 * i + 1], bb.x, bb.y);
+        add2f(v[4 * i + 2], v[4 * i + 3], bb.z, bb.w);
       }
     }
     if (!mbar_wait(&bar[b], (bar_phase >> b) & 1)) atomicOr(status, DEV_TIMEOUT);
@@ -231,10 +227,8 @@ __device__ __forceinline__ void staged_epilogue(const EpiParams& ep, const CUten
 #pragma unroll
       for (int i = 0; i < kCols / 4; ++i) {
         const float4 bb = __ldg(b4 + i);
-        v[4 * i] += bb.x;
-        v[4 * i + 1] += bb.y;
-        v[4 * i + 2] += bb.z;
-        v[4 * i + 3] += bb.w;
+        add2f(v[4 * i], v[4 * i + 1], bb.x, bb.y);
+        add2f(v[4 * i + 2], v[4 * i + 3], bb.z, bb.w);
       }
     }
     if constexpr (EPI == EPI_GELU) {
