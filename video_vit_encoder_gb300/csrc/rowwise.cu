@@ -111,43 +111,54 @@ template <typename T, int NV>
 __global__ void layernorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                  const float* __restrict__ b, T* __restrict__ y, int rows, float eps) {
   constexpr int dim = 128 * NV;
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= rows) return;
-  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)warp * dim);
-  float4 v[NV];
-  float s = 0.f;
+  const int n_warps = (gridDim.x * blockDim.x) >> 5;
+  int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (row >= rows) return;
+  // Each warp walks rows row, row + n_warps, ...; the next row's loads are
+  // issued before the current row is reduced, so two rows are in flight.
+  float4 nxt[NV];
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    v[i] = xr[lane + 32 * i];
-    s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
-  }
-  const float mu = warp_sum(s) * (1.0f / dim);
-  float q = 0.f;
+  for (int i = 0; i < NV; ++i) nxt[i] = reinterpret_cast<const float4*>(x + (size_t)row * dim)[lane + 32 * i];
+  for (; row < rows; row += n_warps) {
+    float4 v[NV];
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    v[i].x -= mu; v[i].y -= mu; v[i].z -= mu; v[i].w -= mu;
-    q += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
-  }
-  const float var = warp_sum(q) * (1.0f / dim);
-  const float rstd = 1.0f / sqrtf(var + eps);
+    for (int i = 0; i < NV; ++i) v[i] = nxt[i];
+    const int next = row + n_warps;
+    if (next < rows) {
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int c = 4 * (lane + 32 * i);
-    const float4 ww = __ldg(reinterpret_cast<const float4*>(w + c));
-    const float4 bb = __ldg(reinterpret_cast<const float4*>(b + c));
-    const float o0 = v[i].x * rstd * ww.x + bb.x;
-    const float o1 = v[i].y * rstd * ww.y + bb.y;
-    const float o2 = v[i].z * rstd * ww.z + bb.z;
-    const float o3 = v[i].w * rstd * ww.w + bb.w;
-    T* yr = y + (size_t)warp * dim + c;
-    if constexpr (sizeof(T) == 2) {
-      uint2 u;
-      u.x = pack2<T>(o0, o1);
-      u.y = pack2<T>(o2, o3);
-      *reinterpret_cast<uint2*>(yr) = u;
-    } else {
-      *reinterpret_cast<float4*>(yr) = make_float4(o0, o1, o2, o3);
+      for (int i = 0; i < NV; ++i) nxt[i] = reinterpret_cast<const float4*>(x + (size_t)next * dim)[lane + 32 * i];
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    const float mu = warp_sum(s) * (1.0f / dim);
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      v[i].x -= mu; v[i].y -= mu; v[i].z -= mu; v[i].w -= mu;
+      q += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
+    }
+    const float var = warp_sum(q) * (1.0f / dim);
+    const float rstd = 1.0f / sqrtf(var + eps);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int c = 4 * (lane + 32 * i);
+      const float4 ww = __ldg(reinterpret_cast<const float4*>(w + c));
+      const float4 bb = __ldg(reinterpret_cast<const float4*>(b + c));
+      const float o0 = v[i].x * rstd * ww.x + bb.x;
+      const float o1 = v[i].y * rstd * ww.y + bb.y;
+      const float o2 = v[i].z * rstd * ww.z + bb.z;
+      const float o3 = v[i].w * rstd * ww.w + bb.w;
+      T* yr = y + (size_t)row * dim + c;
+      if constexpr (sizeof(T) == 2) {
+        uint2 u;
+        u.x = pack2<T>(o0, o1);
+        u.y = pack2<T>(o2, o3);
+        *reinterpret_cast<uint2*>(yr) = u;
+      } else {
+        *reinterpret_cast<float4*>(yr) = make_float4(o0, o1, o2, o3);
+      }
     }
   }
 }
@@ -156,7 +167,15 @@ template <typename T>
 cudaError_t layernorm_t(const float* x, const float* w, const float* b, void* y, int rows, int dim, float eps,
                         cudaStream_t s) {
   const int nv = dim / 128;
-  const int blocks = (rows + 7) / 8;
+  // persistent: 2 blocks of 8 warps per SM, each warp striding over ~rows/2432 rows
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 132;
+  }
+  const int need = (rows + 7) / 8;
+  const int blocks = need < 2 * sms ? need : 2 * sms;
   T* yy = reinterpret_cast<T*>(y);
   switch (nv) {
     case 1: layernorm_kernel<T, 1><<<blocks, 256, 0, s>>>(x, w, b, yy, rows, eps); break;
