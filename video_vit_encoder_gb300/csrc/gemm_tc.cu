@@ -39,6 +39,32 @@ struct GemmSmem {
   static constexpr size_t kBytes = 1024 /*alignment slack*/ + kBarOffset + 320;
 };
 
+// Writes the staged head rows of one warp (32 rows from row0, head `head` of
+// the q (which 0) or k (which 1) section) to the head-major output: HD x 2
+// bytes per token, a row's token and clip taken from its own index, so the 32
+// rows may span two clips.  Rows at or past M are not written.
+template <typename T, int HD>
+__device__ __forceinline__ void stage_out_head(const EpiParams& ep, int which, uint8_t* stage, int row0, int head,
+                                               int M, int lane) {
+  constexpr int kSeg = HD * 2 / 16;        // 16-byte segments per head row
+  constexpr int kRowsPer = 32 / kSeg;      // rows per warp instruction
+  __syncwarp();
+  T* base = reinterpret_cast<T*>(which == 0 ? ep.q : ep.k);
+#pragma unroll
+  for (int it = 0; it < kSeg; ++it) {
+    const int r = it * kRowsPer + lane / kSeg, g = lane % kSeg;
+    const int grow = row0 + r;
+    const uint4 u = reinterpret_cast<const uint4*>(stage + r * 128)[g ^ (r & 7)];
+    if (grow < M) {
+      const int clip = grow / ep.n_tok;
+      const int tok = grow - clip * ep.n_tok;
+      const size_t bh = (size_t)clip * ep.n_head + head;
+      reinterpret_cast<uint4*>(base + (bh * ep.n_tok + tok) * HD)[g] = u;
+    }
+  }
+  __syncwarp();   // the buffer is reused for the next head
+}
+
 // QKV epilogue of one thread's row of a 128 x BN accumulator tile.  BN
 // divides D, so the whole tile lies in the q, the k or the v section.  The
 // token's RoPE factors (3 axes x d/2 angles, cos and sin) are loaded once per
@@ -48,9 +74,15 @@ struct GemmSmem {
 //   out[2k+1] = x[2k+1] cos(a_f1) + x[2k]   sin(a_f1)
 // with f0 = f1 = k' (interleaved) or f0 = 2k' mod d/2, f1 = (2k'+1) mod d/2
 // (tiled), k' the pair index within its axis segment.
+//
+// q and k rows leave through the warp's 4 KB staging buffer: each thread puts
+// its head row there (16-byte segments XOR-swizzled by row, so neither side
+// has bank conflicts), and the warp then writes whole 128-byte head rows of
+// consecutive tokens, one full line per eight lanes, instead of each thread
+// writing a half sector of 32 different lines.
 template <typename T, int BN, int HD, int LAYOUT>
 __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t taddr, int row, bool row_ok,
-                                                  int col_base, int col_off) {
+                                                  int col_base, int col_off, uint8_t* stage, int M, int lane) {
   static_assert(HD == 32 || HD == 64, "head dim");
   static_assert((BN / 2) % HD == 0, "each half tile must hold whole heads");
   constexpr int RD = 2 * ((HD / 3) / 2);
@@ -89,6 +121,13 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_wait_ld();
+    const int d0 = (c * 32) % HD;
+    const size_t bh = bh0 + (c * 32) / HD;
+    if (which < 2 && !row_ok) {
+      // the warp still takes part in the staged store of this head
+      if (d0 + 32 == HD) stage_out_head<T, HD>(ep, which, stage, row - lane, (int)(bh - bh0) + head0, M, lane);
+      continue;
+    }
     if (!row_ok) continue;
     float v[32];
 #pragma unroll
@@ -102,8 +141,6 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
         add2f(v[i + 2], v[i + 3], bb.z, bb.w);
       }
     }
-    const int d0 = (c * 32) % HD;
-    const size_t bh = bh0 + (c * 32) / HD;
     if (which < 2) {
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
@@ -118,8 +155,17 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
           v[j + 1] = x1 * cz[a][f1] + x0 * sz[a][f1];
         }
       }
-      T* dst = reinterpret_cast<T*>(which == 0 ? ep.q : ep.k) + (bh * ep.n_tok + tok) * HD + d0;
-      store_row_chunk<T, 32>(dst, v);
+      uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 u;
+        u.x = pack2<T>(v[8 * i + 0], v[8 * i + 1]);
+        u.y = pack2<T>(v[8 * i + 2], v[8 * i + 3]);
+        u.z = pack2<T>(v[8 * i + 4], v[8 * i + 5]);
+        u.w = pack2<T>(v[8 * i + 6], v[8 * i + 7]);
+        srow[(d0 / 8 + i) ^ (lane & 7)] = u;
+      }
+      if (d0 + 32 == HD) stage_out_head<T, HD>(ep, which, stage, row - lane, (int)(bh - bh0) + head0, M, lane);
     } else {
       T* dst = reinterpret_cast<T*>(ep.vt) + (bh * HD + d0) * (size_t)ep.ldv + tok;
 #pragma unroll
@@ -475,7 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (EPI == EPI_QKV) {
         qkv_tile_epilogue<T, BN, QHD, QLAYOUT>(ep, tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN +
                                                    half * (BN / 2),
-                                               row, row < M, tn * BN, half * (BN / 2));
+                                               row, row < M, tn * BN, half * (BN / 2),
+                                               sEpi + (warp - 2) * S::kEpiStage, M, lane);
       } else if constexpr (EPI == EPI_RESID && EBUF == 2) {
         resid_epilogue<BN / 2>(ep, &tmC, tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2),
                                row - lane, tn * BN + half * (BN / 2), sEpi + (warp - 2) * S::kEpiStage,
