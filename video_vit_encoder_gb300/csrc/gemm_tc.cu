@@ -27,13 +27,13 @@ constexpr int kBK = 64;  // 64 x 16-bit = one 128-byte swizzle row
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;   // warps 2-9
 
-template <int BN, int STAGES, int CM, int EBUF = 1>
+template <int BN, int STAGES, int CM>
 struct GemmSmem {
   static constexpr uint32_t kABytes = kBM * kBK * 2;          // this CTA's 128 rows of A
   static constexpr uint32_t kBBytes = (BN / CM) * kBK * 2;    // this CTA's rows of W
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; a power of two
-  static constexpr uint32_t kEpiStage = 4096 * EBUF;  // per epilogue warp: EBUF x (32 rows x 128 bytes)
+  static constexpr uint32_t kEpiStage = 4096;  // per epilogue warp: 32 rows x 128 bytes
   static constexpr uint32_t kEpiOffset = STAGES * kStageBytes;
   static constexpr uint32_t kBarOffset = kEpiOffset + (kEpiThreads / 32) * kEpiStage;
   static constexpr size_t kBytes = 1024 /*alignment slack*/ + kBarOffset + 320;
@@ -174,33 +174,18 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
   }
 }
 
-// Residual epilogue of one warp for rows row0 .. row0+31 of the tile and
-// NCOLS fp32 columns from col0: out = residual + accumulator (+ bias), in
-// place.  The residual arrives by TMA in 32 x 128-byte blocks into two
-// alternating staging buffers, the next block requested before the current
-// one is added, and each sum leaves by one TMA tensor store.  bar[0..1] are
-// the buffers' arrival barriers; bit b of bar_phase is buffer b's parity.
+// Residual epilogue by reduction, for rows row0 .. row0+31 of the tile and
+// NCOLS fp32 columns from col0: accumulator (+ bias) -> a 32 x 128-byte
+// staging block in the 128B swizzle -> one TMA reduce-add per block into the
+// output, which holds the residual: out = residual + (accumulator + bias),
+// one fp32 addition per element performed by L2.  The warp's next block waits
+// only until the previous reduction has read the buffer, not for its writes.
 template <int NCOLS>
-__device__ __forceinline__ void resid_epilogue(const EpiParams& ep, const CUtensorMap* tmC, uint32_t taddr, int row0,
-                                               int col0, uint8_t* buf, uint64_t* bar, uint32_t& bar_phase, int lane,
-                                               int* status) {
+__device__ __forceinline__ void reduce_epilogue(const EpiParams& ep, const CUtensorMap* tmC, uint32_t taddr, int row0,
+                                                int col0, uint8_t* buf, int lane) {
   constexpr int kCols = 32;  // fp32 columns per 128-byte block
-  constexpr int kBlocks = NCOLS / kCols;
-  if (lane == 0) {
-    bulk_wait_read_all();  // stores of the previous tile have left both buffers
-    mbar_arrive_expect_tx(&bar[0], 4096);
-    tma_load_2d(buf, tmC, &bar[0], col0, row0);
-  }
 #pragma unroll 1
-  for (int c = 0; c < kBlocks; ++c) {
-    const int b = c & 1;
-    uint8_t* cur = buf + b * 4096;
-    if (c + 1 < kBlocks && lane == 0) {
-      // buffer b^1 was last stored from at block c-1: wait for that read
-      bulk_wait_read_all();
-      mbar_arrive_expect_tx(&bar[b ^ 1], 4096);
-      tma_load_2d(buf + (b ^ 1) * 4096, tmC, &bar[b ^ 1], col0 + (c + 1) * kCols, row0);
-    }
+  for (int c = 0; c < NCOLS / kCols; ++c) {
     float v[kCols];
     {
       uint32_t r[32];
@@ -218,47 +203,37 @@ __device__ __forceinline__ void resid_epilogue(const EpiParams& ep, const CUtens
         add2f(v[4 * i + 2], v[4 * i + 3], bb.z, bb.w);
       }
     }
-    if (!mbar_wait(&bar[b], (bar_phase >> b) & 1)) atomicOr(status, DEV_TIMEOUT);
-    bar_phase ^= 1u << b;
-    uint8_t* my_row = cur + lane * 128;
+    // the previous block's reduction has read the buffer
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+    uint8_t* my_row = buf + lane * 128;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      float4* p = reinterpret_cast<float4*>(my_row + ((k ^ (lane & 7)) << 4));
-      const float4 x = *p;
-      *p = make_float4(x.x + v[4 * k], x.y + v[4 * k + 1], x.z + v[4 * k + 2], x.w + v[4 * k + 3]);
-    }
+    for (int k = 0; k < 8; ++k)
+      *reinterpret_cast<float4*>(my_row + ((k ^ (lane & 7)) << 4)) =
+          make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
     fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(tmC, cur, col0 + c * kCols, row0);
+      tma_reduce_add_2d(tmC, buf, col0 + c * kCols, row0);
       bulk_commit_group();
     }
   }
 }
 
 // Epilogue of one warp for rows row0 .. row0+31 of the tile (its TMEM lanes)
-// and NCOLS columns from col0: accumulator (+ bias, activation; + the
-// residual for EPI_RESID) -> a 32 x 128-byte staging buffer in the 128B
-// swizzle -> one TMA tensor store per 128-byte column block, so global memory
-// sees whole rows instead of one row per lane.  The residual block arrives by
-// TMA into the same buffer, requested before the accumulator is read.  Rows
-// and columns outside the output are clipped by the tensor map.
+// and NCOLS columns from col0: accumulator (+ bias, activation) -> a 32 x
+// 128-byte staging buffer in the 128B swizzle -> one TMA tensor store per
+// 128-byte column block, so global memory sees whole rows instead of one row
+// per lane.  Rows and columns outside the output are clipped by the tensor map.
 template <typename T, int EPI, int NCOLS>
 __device__ __forceinline__ void staged_epilogue(const EpiParams& ep, const CUtensorMap* tmC, uint32_t taddr, int row0,
-                                                int col0, uint8_t* buf, uint64_t* bar, uint32_t& bar_phase, int lane,
-                                                int* status) {
-  constexpr bool kF32Out = EPI == EPI_F32 || EPI == EPI_RESID;
+                                                int col0, uint8_t* buf, int lane) {
+  static_assert(EPI == EPI_STORE || EPI == EPI_F32 || EPI == EPI_GELU, "staged epilogue");
+  constexpr bool kF32Out = EPI == EPI_F32;
   constexpr int kCols = kF32Out ? 32 : 64;  // columns per 128-byte block
   uint8_t* my_row = buf + lane * 128;
 #pragma unroll 1
   for (int c0 = 0; c0 < NCOLS; c0 += kCols) {
-    if constexpr (EPI == EPI_RESID) {
-      if (lane == 0) {
-        bulk_wait_read_all();  // the previous block's store has left the buffer
-        mbar_arrive_expect_tx(bar, 4096);
-        tma_load_2d(buf, tmC, bar, col0 + c0, row0);
-      }
-    }
     float v[kCols];
 #pragma unroll
     for (int h = 0; h < kCols / 32; ++h) {
@@ -281,30 +256,19 @@ __device__ __forceinline__ void staged_epilogue(const EpiParams& ep, const CUten
 #pragma unroll
       for (int i = 0; i < kCols; i += 2) gelu_as2(v[i], v[i + 1]);
     }
-    if constexpr (EPI == EPI_RESID) {
-      if (!mbar_wait(bar, bar_phase)) atomicOr(status, DEV_TIMEOUT);
-      bar_phase ^= 1;
+    if (lane == 0) bulk_wait_read_all();  // the previous block's store has left the buffer
+    __syncwarp();
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float4* p = reinterpret_cast<float4*>(my_row + ((k ^ (lane & 7)) << 4));
-        const float4 x = *p;
-        *p = make_float4(x.x + v[4 * k], x.y + v[4 * k + 1], x.z + v[4 * k + 2], x.w + v[4 * k + 3]);
+    for (int k = 0; k < 8; ++k) {
+      uint4 w;
+      if constexpr (kF32Out) {
+        w = make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
+                       __float_as_uint(v[4 * k + 3]));
+      } else {
+        w = make_uint4(pack2<T>(v[8 * k], v[8 * k + 1]), pack2<T>(v[8 * k + 2], v[8 * k + 3]),
+                       pack2<T>(v[8 * k + 4], v[8 * k + 5]), pack2<T>(v[8 * k + 6], v[8 * k + 7]));
       }
-    } else {
-      if (lane == 0) bulk_wait_read_all();
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        uint4 w;
-        if constexpr (kF32Out) {
-          w = make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
-                         __float_as_uint(v[4 * k + 3]));
-        } else {
-          w = make_uint4(pack2<T>(v[8 * k], v[8 * k + 1]), pack2<T>(v[8 * k + 2], v[8 * k + 3]),
-                         pack2<T>(v[8 * k + 4], v[8 * k + 5]), pack2<T>(v[8 * k + 6], v[8 * k + 7]));
-        }
-        *reinterpret_cast<uint4*>(my_row + ((k ^ (lane & 7)) << 4)) = w;
-      }
+      *reinterpret_cast<uint4*>(my_row + ((k ^ (lane & 7)) << 4)) = w;
     }
     fence_proxy_async_shared();
     __syncwarp();
@@ -315,23 +279,22 @@ __device__ __forceinline__ void staged_epilogue(const EpiParams& ep, const CUten
   }
 }
 
-template <typename T, int BN, int STAGES, int EPI, int QHD = 0, int QLAYOUT = 0, int CM = 1, int EBUF = 1>
+template <typename T, int BN, int STAGES, int EPI, int QHD = 0, int QLAYOUT = 0, int CM = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, int M, int N, int K, EpiParams ep, int* status) {
-  using S = GemmSmem<BN, STAGES, CM, EBUF>;
+  using S = GemmSmem<BN, STAGES, CM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * S::kABytes;
-  uint8_t* sEpi = smem + S::kEpiOffset;  // epilogue staging, one or two 4 KB buffers per epilogue warp
+  uint8_t* sEpi = smem + S::kEpiOffset;  // epilogue staging, one 4 KB buffer per epilogue warp
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOffset);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;  // [2] accumulator ready for the epilogue
   uint64_t* tempty = tfull + 2;      // [2] accumulator drained by the epilogue
   uint64_t* mma_done = tempty + 2;
-  uint64_t* epi_bar = mma_done + 1;  // [8][2] residual arrivals, two per epilogue warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 2 * (kEpiThreads / 32));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -358,7 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[i], CM * (kEpiThreads / 32));   // one arrival per epilogue warp of every CTA
     }
     mbar_init(mma_done, 1);
-    for (int i = 0; i < 2 * (kEpiThreads / 32); ++i) mbar_init(&epi_bar[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -503,7 +465,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t tempty0 = CM == 2 ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
-    uint32_t epi_phase = 0;
     int acc = 0;
     for (int u = first_unit; u < num_units; u += unit_stride, ++acc) {
       const int buf = acc & 1;
@@ -523,15 +484,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    half * (BN / 2),
                                                row, row < M, tn * BN, half * (BN / 2),
                                                sEpi + (warp - 2) * S::kEpiStage, M, lane);
-      } else if constexpr (EPI == EPI_RESID && EBUF == 2) {
-        resid_epilogue<BN / 2>(ep, &tmC, tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2),
-                               row - lane, tn * BN + half * (BN / 2), sEpi + (warp - 2) * S::kEpiStage,
-                               &epi_bar[2 * (warp - 2)], epi_phase, lane, status);
+      } else if constexpr (EPI == EPI_RESID) {
+        reduce_epilogue<BN / 2>(ep, &tmC,
+                                      tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2),
+                                      row - lane, tn * BN + half * (BN / 2), sEpi + (warp - 2) * S::kEpiStage, lane);
       } else {
         staged_epilogue<T, EPI, BN / 2>(ep, &tmC,
                                         tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2),
                                         row - lane, tn * BN + half * (BN / 2), sEpi + (warp - 2) * S::kEpiStage,
-                                        &epi_bar[2 * (warp - 2)], epi_phase, lane, status);
+                                        lane);
       }
       tc_fence_before();
       __syncwarp();
@@ -559,11 +520,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename T, int BN, int STAGES, int CM, int EPI, int QHD = 0, int QLAYOUT = 0, int EBUF = 1>
+template <typename T, int BN, int STAGES, int CM, int EPI, int QHD = 0, int QLAYOUT = 0>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, int M, int N, int K,
                        const EpiParams& ep, int* status, cudaStream_t stream, int num_sms) {
-  using S = GemmSmem<BN, STAGES, CM, EBUF>;
-  auto kern = gemm_tc_kernel<T, BN, STAGES, EPI, QHD, QLAYOUT, CM, EBUF>;
+  using S = GemmSmem<BN, STAGES, CM>;
+  auto kern = gemm_tc_kernel<T, BN, STAGES, EPI, QHD, QLAYOUT, CM>;
   static bool configured = false;  // per instantiation
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
@@ -607,16 +568,7 @@ cudaError_t dispatch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, 
   switch (epi) {
     case EPI_STORE: return launch_one<T, BN, STAGES, CM, EPI_STORE>(ta, tb, tc, M, N, K, ep, status, s, sms);
     case EPI_F32: return launch_one<T, BN, STAGES, CM, EPI_F32>(ta, tb, tc, M, N, K, ep, status, s, sms);
-    case EPI_RESID: {
-      // Short K: the epilogue dominates, so it gets two staging buffers per
-      // warp and the main loop as many stages as still fit.
-      if (K > 2048) return launch_one<T, BN, STAGES, CM, EPI_RESID>(ta, tb, tc, M, N, K, ep, status, s, sms);
-      constexpr int kStage = kBM * kBK * 2 + (BN / CM) * kBK * 2;
-      constexpr int kFit = (227 * 1024 - 1024 - 320 - (kEpiThreads / 32) * 8192) / kStage;
-      constexpr int kSt = kFit < STAGES ? kFit : STAGES;
-      static_assert(kSt >= 2, "residual epilogue leaves too little shared memory");
-      return launch_one<T, BN, kSt, CM, EPI_RESID, 0, 0, 2>(ta, tb, tc, M, N, K, ep, status, s, sms);
-    }
+    case EPI_RESID: return launch_one<T, BN, STAGES, CM, EPI_RESID>(ta, tb, tc, M, N, K, ep, status, s, sms);
     case EPI_GELU: return launch_one<T, BN, STAGES, CM, EPI_GELU>(ta, tb, tc, M, N, K, ep, status, s, sms);
     case EPI_QKV:
       if (ep.head_dim == 64)
