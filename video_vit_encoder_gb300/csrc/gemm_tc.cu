@@ -108,10 +108,23 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
     for (int a = 0; a < 3; ++a) {
       const float* ct = ep.rope.cos_tab + (a * ep.rope.max_pos + p[a]) * HALF;
       const float* st = ep.rope.sin_tab + (a * ep.rope.max_pos + p[a]) * HALF;
+      if constexpr (HALF % 2 == 0) {
+        // rows of an even number of floats start on 8 bytes: two angles per load
 #pragma unroll
-      for (int k = 0; k < HALF; ++k) {
-        cz[a][k] = __ldg(ct + k);
-        sz[a][k] = __ldg(st + k);
+        for (int k = 0; k < HALF; k += 2) {
+          const float2 cc = __ldg(reinterpret_cast<const float2*>(ct + k));
+          const float2 ss = __ldg(reinterpret_cast<const float2*>(st + k));
+          cz[a][k] = cc.x;
+          cz[a][k + 1] = cc.y;
+          sz[a][k] = ss.x;
+          sz[a][k + 1] = ss.y;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < HALF; ++k) {
+          cz[a][k] = __ldg(ct + k);
+          sz[a][k] = __ldg(st + k);
+        }
       }
     }
   }
