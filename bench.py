@@ -49,7 +49,16 @@ WORKLOADS = {
                       "bf16 tensor peak",
                       "ViT-B/16 12L D768 h12 FFN3072, bf16, 2.1 native image path (tubelet 1, patch_embed_img), "
                       "interleaved interpolated RoPE, 1f x 384x384 (576 tokens/image), batch 32 per GPU", None),
+    "vitl16-64f256": ("c4", "encoder tokens/sec (ViT-L/16, 64f 256px, bf16) and % of bf16 tensor peak",
+                      "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 64f x 256x256 (8192 tokens/clip), "
+                      "batch 1 per GPU", None),
+    "vitb16-64f384": ("c5", "encoder tokens/sec (V-JEPA 2.1 ViT-B/16, 64f 384px, bf16) and % of bf16 tensor peak",
+                      "ViT-B/16 12L D768 h12 FFN3072, bf16, interleaved interpolated RoPE, 64f x 384x384 "
+                      "(18432 tokens/clip), batch 1 per GPU", None),
 }
+# The oracle holds each head's full score matrix in float64; above this many
+# tokens per clip one of its blocks no longer fits a bounded CPU sample.
+CPU_BASELINE_MAX_TOKENS = 8192
 DEFAULT_WORKLOAD = "vitl16-16f256"
 CLASSES = ["patch_embed", "layernorm", "qkv_gemm", "attention", "out_proj_gemm", "ffn_up_gemm", "ffn_down_gemm",
            "other"]
@@ -219,6 +228,10 @@ def run_reference(args):
         print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the unmasked workloads only"}))
         return 0
     cfg = synth.CONFIGS[key]
+    if synth.tokens_per_clip(cfg) > CPU_BASELINE_MAX_TOKENS:
+        print(json.dumps({"impl": "reference", "unavailable": f"one oracle block at {synth.tokens_per_clip(cfg)} "
+                          "tokens per clip takes minutes on the host cores (float64 score matrices)"}))
+        return 0
     w = synth.encoder_weights(cfg)
     clip = synth.clip_u8(cfg, batch=1)[0]
     vals = []
@@ -394,8 +407,14 @@ def main():
                                     "what": "pages' ggml-CUDA f16 ViT-L/16 16f 256px, batch 1, RTX 4500 Ada "
                                             "(context only)"}
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, weights, clip_np[0], blocks=4)
-        line["cpu_baseline"].pop("seconds_per_clip", None)
+        if synth.tokens_per_clip(cfg) > CPU_BASELINE_MAX_TOKENS:
+            line["cpu_baseline"] = {"value": None, "unit": UNIT, "kind": "oracle",
+                                    "sample": "not run: one oracle block at this clip length takes minutes "
+                                              "on the host cores (float64 score matrices)"}
+        else:
+            n_blocks = 4 if synth.tokens_per_clip(cfg) <= 2048 else 1
+            line["cpu_baseline"] = cpu_baseline(cfg, weights, clip_np[0], blocks=n_blocks)
+            line["cpu_baseline"].pop("seconds_per_clip", None)
     enc.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
