@@ -292,10 +292,38 @@ __device__ __forceinline__ void staged_epilogue(const EpiParams& ep, const CUten
   }
 }
 
+// Tile of work unit u: its row-tile group mp, column tile tn, first output
+// column col0 and width (BN, or BN/2 for a half of a split tail tile).
+struct UnitTile {
+  int mp, tn, col0, width;
+};
+template <int BN>
+__device__ __forceinline__ UnitTile unit_tile(int u, int num_n, int tail_start) {
+  UnitTile t;
+  const int tile = u < tail_start ? u : tail_start + ((u - tail_start) >> 1);
+  t.mp = tile / num_n;
+  t.tn = tile - t.mp * num_n;
+  t.width = u < tail_start ? BN : BN / 2;
+  t.col0 = t.tn * BN + (u < tail_start ? 0 : ((u - tail_start) & 1) * (BN / 2));
+  return t;
+}
+
+// Whether an instantiation's epilogue can take a half-width (BN/2) tile: each
+// epilogue warp then covers BN/4 columns, which must hold whole 128-byte
+// output blocks.  The QKV epilogue is not split: a second inlined copy of it
+// does not fit the epilogue warps' registers.
+template <int BN, int EPI, int QHD>
+__host__ __device__ constexpr bool can_split_tail() {
+  if constexpr (EPI == EPI_QKV) return false;
+  if constexpr (EPI == EPI_RESID || EPI == EPI_F32) return (BN / 4) % 32 == 0;
+  return (BN / 4) % 64 == 0;
+}
+
 template <typename T, int BN, int STAGES, int EPI, int QHD = 0, int QLAYOUT = 0, int CM = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, EpiParams ep, int* status) {
+                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int tail_start, EpiParams ep,
+                   int* status) {
   using S = GemmSmem<BN, STAGES, CM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -317,7 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // CTA pair (CM = 2) the even CTA issues one M = 256 MMA per K step over both
   // CTAs' shared memory; each CTA holds its 128 rows of A and half of the W
   // tile and receives its 128 rows of the accumulator in its tensor memory.
-  const int num_units = ((M + kBM * CM - 1) / (kBM * CM)) * num_n;
+  // Units from tail_start on are the tiles of the last, partial wave, each
+  // split into two BN/2-wide halves run by different CTAs (pairs), so that
+  // wave takes about half as long; tail_start = the unit count means no split.
+  const int num_tiles = ((M + kBM * CM - 1) / (kBM * CM)) * num_n;
+  const int num_units = tail_start + 2 * (num_tiles - tail_start);
   const int num_kb = K / kBK;
   const int rank = CM == 2 ? (int)cluster_ctarank() : 0;
   const bool leader = rank == 0;
@@ -366,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       long issued = 0;
       for (int u = first_unit; u < num_units && !*abort_flag; u += unit_stride) {
-        const int mp = u / num_n, tn = u - mp * num_n;
-        const int tm = mp * CM + rank;
+        const UnitTile ut = unit_tile<BN>(u, num_n, tail_start);
+        const int tm = ut.mp * CM + rank;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             atomicOr(status, DEV_TIMEOUT);
@@ -377,11 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (CM == 2) {
             if (leader) mbar_arrive_expect_tx(&full[stage], 2 * S::kStageBytes);
             tma_load_2d_pair(sA + stage * S::kABytes, &tmA, full0 + 8 * stage, kb * kBK, tm * kBM);
-            tma_load_2d_pair(sB + stage * S::kBBytes, &tmB, full0 + 8 * stage, kb * kBK, tn * BN + rank * (BN / 2));
+            // each CTA holds width/2 rows of W (a half tile leaves the rest of the box unused)
+            tma_load_2d_pair(sB + stage * S::kBBytes, &tmB, full0 + 8 * stage, kb * kBK, ut.col0 + rank * (ut.width / 2));
           } else {
             mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
             tma_load_2d(sA + stage * S::kABytes, &tmA, &full[stage], kb * kBK, tm * kBM);
-            tma_load_2d(sB + stage * S::kBBytes, &tmB, &full[stage], kb * kBK, tn * BN);
+            tma_load_2d(sB + stage * S::kBBytes, &tmB, &full[stage], kb * kBK, ut.col0);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -409,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp walks the schedule (waits are warp-uniform); one elected
     // lane issues each MMA and commit.
     if (leader) {
-      constexpr uint32_t idesc = idesc_f16<T, kBM * CM, BN>();
+      constexpr uint32_t idesc_full = idesc_f16<T, kBM * CM, BN>();
+      constexpr uint32_t idesc_half = idesc_f16<T, kBM * CM, BN / 2>();
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -424,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN;
+        const uint32_t idesc = u < tail_start ? idesc_full : idesc_half;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase))) {
             ok = false;
@@ -490,22 +525,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int mp = u / num_n, tn = u - mp * num_n;
-      const int row = (mp * CM + rank) * kBM + row_in_tile;
-      if constexpr (EPI == EPI_QKV) {
-        qkv_tile_epilogue<T, BN, QHD, QLAYOUT>(ep, tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN +
-                                                   half * (BN / 2),
-                                               row, row < M, tn * BN, half * (BN / 2),
-                                               sEpi + (warp - 2) * S::kEpiStage, M, lane);
-      } else if constexpr (EPI == EPI_RESID) {
-        reduce_epilogue<BN / 2>(ep, &tmC,
-                                      tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2),
-                                      row - lane, tn * BN + half * (BN / 2), sEpi + (warp - 2) * S::kEpiStage, lane);
-      } else {
-        staged_epilogue<T, EPI, BN / 2>(ep, &tmC,
-                                        tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2),
-                                        row - lane, tn * BN + half * (BN / 2), sEpi + (warp - 2) * S::kEpiStage,
-                                        lane);
+      const UnitTile ut = unit_tile<BN>(u, num_n, tail_start);
+      const int row = (ut.mp * CM + rank) * kBM + row_in_tile;
+      const uint32_t tlane = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN;
+      uint8_t* stage_buf = sEpi + (warp - 2) * S::kEpiStage;
+      if (ut.width == BN) {
+        if constexpr (EPI == EPI_QKV) {
+          qkv_tile_epilogue<T, BN, QHD, QLAYOUT>(ep, tlane + half * (BN / 2), row, row < M, ut.col0, half * (BN / 2),
+                                                 stage_buf, M, lane);
+        } else if constexpr (EPI == EPI_RESID) {
+          reduce_epilogue<BN / 2>(ep, &tmC, tlane + half * (BN / 2), row - lane, ut.col0 + half * (BN / 2), stage_buf,
+                                  lane);
+        } else {
+          staged_epilogue<T, EPI, BN / 2>(ep, &tmC, tlane + half * (BN / 2), row - lane, ut.col0 + half * (BN / 2),
+                                          stage_buf, lane);
+        }
+      } else if constexpr (can_split_tail<BN, EPI, QHD>()) {
+        // half-width tail tile: each warp drains BN/4 columns
+        if constexpr (EPI == EPI_RESID) {
+          reduce_epilogue<BN / 4>(ep, &tmC, tlane + half * (BN / 4), row - lane, ut.col0 + half * (BN / 4), stage_buf,
+                                  lane);
+        } else {
+          staged_epilogue<T, EPI, BN / 4>(ep, &tmC, tlane + half * (BN / 4), row - lane, ut.col0 + half * (BN / 4),
+                                          stage_buf, lane);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -530,6 +573,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       tmem_dealloc(tmem_base, S::kTmemCols);
     }
+  }
+}
+
+// First tile of the last wave to split into halves: the tiles beyond the last
+// full wave of `slots` resident CTAs (pairs), when twice their count still fits
+// in one wave and the epilogue takes half tiles; otherwise `tiles` (no split).
+template <int BN, int EPI, int QHD>
+int split_tail_start(int tiles, int slots) {
+  if constexpr (!can_split_tail<BN, EPI, QHD>()) {
+    return tiles;
+  } else {
+    const int rem = tiles % slots;
+    if (rem == 0 || 2 * rem > slots) return tiles;
+    return tiles - rem;
   }
 }
 
@@ -563,14 +620,18 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
       cfg.gridDim = dim3(2 * (num_sms / 2));
       if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) resident = num_sms / 2;
     }
-    const int units = ((num_m + 1) / 2) * num_n;
+    const int tiles = ((num_m + 1) / 2) * num_n;
+    const int tail_start = split_tail_start<BN, EPI, QHD>(tiles, resident);
+    const int units = tail_start + 2 * (tiles - tail_start);
     const int clusters = units < resident ? units : resident;
     cfg.gridDim = dim3(2 * clusters);
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, M, N, K, ep, status);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, M, N, K, tail_start, ep, status);
   } else {
     const int tiles = num_m * num_n;
-    const int grid = tiles < num_sms ? tiles : num_sms;
-    kern<<<grid, kThreads, S::kBytes, stream>>>(ta, tb, tc, M, N, K, ep, status);
+    const int tail_start = split_tail_start<BN, EPI, QHD>(tiles, num_sms);
+    const int units = tail_start + 2 * (tiles - tail_start);
+    const int grid = units < num_sms ? units : num_sms;
+    kern<<<grid, kThreads, S::kBytes, stream>>>(ta, tb, tc, M, N, K, tail_start, ep, status);
     return cudaGetLastError();
   }
 }
