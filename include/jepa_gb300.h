@@ -35,7 +35,8 @@
 extern "C" {
 #endif
 
-#define JEPA_ABI_VERSION 3  /* 2: jepa_encoder_params.has_image_path; 3: 2.1 predictor fields */
+#define JEPA_ABI_VERSION 4  /* 2: jepa_encoder_params.has_image_path; 3: 2.1 predictor fields;
+                               4: jepa_encode_host_async */
 
 #if defined(__GNUC__)
 #define JEPA_API __attribute__((visibility("default")))
@@ -189,6 +190,23 @@ JEPA_API jepa_status jepa_encode_host(jepa_encoder* enc, const void* host_clip, 
                              int n_frames, int height, int width, float* host_out_tokens,
                              float* host_out_pooled, void* stream);
 
+/* Streaming form of jepa_encode_host for a sequence of clips: enqueues the
+ * copy of host_clip to the device, the encode on `stream` and the copy of the
+ * result to host_out_tokens (and host_out_pooled if not NULL), and returns
+ * without waiting.  Consecutive calls use two device staging slots in turn,
+ * and the copies run on two streams of the handle, so one call's copy-in and
+ * the previous call's copy-out overlap the encodes.  Events order each slot's
+ * reuse: a slot's clip is overwritten only after the encode that read it, and
+ * its output only after the copy that read it.
+ * The caller keeps host_clip unchanged, and reads neither host output, until
+ * jepa_encoder_sync(enc, stream) returns; that call waits for the copies too
+ * and reports device-side errors.  Pinned host memory makes the copies truly
+ * asynchronous; pageable memory still gives correct results.  Arguments and
+ * errors found on the host are those of jepa_encode_host. */
+JEPA_API jepa_status jepa_encode_host_async(jepa_encoder* enc, const void* host_clip, int clip_format, int batch,
+                                            int n_frames, int height, int width, float* host_out_tokens,
+                                            float* host_out_pooled, void* stream);
+
 /* The two halves of jepa_encode, for checking one stage at a time:
  * jepa_encoder_embed writes the patch embedding (+ modality vector) of the
  * clip into x_out, device float [batch*N, D]; jepa_encoder_blocks runs blocks
@@ -199,8 +217,9 @@ JEPA_API jepa_status jepa_encoder_embed(jepa_encoder* enc, const void* clip, int
 JEPA_API jepa_status jepa_encoder_blocks(jepa_encoder* enc, float* x, int batch, int n_frames, int height, int width,
                                 int layer_begin, int layer_end, void* stream);
 
-/* Synchronises `stream` and reports a device-side timeout recorded by any
- * earlier call on this handle (then clears it). */
+/* Synchronises `stream` (and the copy streams of jepa_encode_host_async) and
+ * reports a device-side timeout recorded by any earlier call on this handle
+ * (then clears it). */
 JEPA_API jepa_status jepa_encoder_sync(jepa_encoder* enc, void* stream);
 
 /* Per-kernel-class device time of the calls made while profiling is on,

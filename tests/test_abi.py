@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
         assert n in SIGNATURES, f"binding lacks {n}"
-    assert lib.jepa_abi_version() == 3
+    assert lib.jepa_abi_version() == 4
 
 
 def _blob(cfg):
@@ -116,6 +116,7 @@ def test_argument_errors_without_gpu(lib):
     assert lib.jepa_attention(C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), 2, 1, 1, 100, 64,
                               100, 0.125, None) == ERR_ARG          # ldv not a multiple of 8
     assert lib.jepa_encoder_sync(None, None) == ERR_ARG
+    assert lib.jepa_encode_host_async(None, C.c_void_p(16), 0, 1, 2, 16, 16, C.c_void_p(16), None, None) == ERR_ARG
     assert b"NULL" in lib.jepa_last_error()
 
 

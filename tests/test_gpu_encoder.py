@@ -102,6 +102,34 @@ def test_encode_host_matches_device(jg):
     enc.close()
 
 
+def test_encode_host_async_stream_of_clips(jg):
+    """Five different clips streamed through jepa_encode_host_async (two
+    staging slots used in turn, copies on the handle's own streams) each give
+    exactly the device-buffer encode of that clip; a shape change in the middle
+    of the stream reallocates a slot only after its earlier work is done."""
+    cfg = SMALL["v2-hd32"]
+    w = synth.encoder_weights(cfg)
+    enc = jg.Encoder(cfg, w)
+    rng = np.random.default_rng(11)
+    shapes = [(2, 4, 64, 64), (2, 4, 64, 64), (1, 4, 64, 64), (2, 4, 64, 80), (2, 4, 64, 64)]
+    clips = [rng.integers(0, 256, (B, T, H, W, 3), dtype=np.uint8) for B, T, H, W in shapes]
+    want, hin, hout, hpool = [], [], [], []
+    for c in clips:
+        d = enc.encode(torch.from_numpy(c).cuda(), pooled=True)
+        enc.sync()
+        want.append((d["out"].cpu(), d["pooled"].cpu()))
+        hin.append(torch.from_numpy(c).pin_memory())
+        hout.append(torch.empty(d["out"].shape, dtype=torch.float32).pin_memory())
+        hpool.append(torch.empty(d["pooled"].shape, dtype=torch.float32).pin_memory())
+    for i in range(len(clips)):
+        enc.encode_host_async(hin[i], hout[i], hpool[i])
+    enc.sync()
+    for i in range(len(clips)):
+        assert torch.equal(hout[i], want[i][0]), i
+        assert torch.equal(hpool[i], want[i][1]), i
+    enc.close()
+
+
 def test_batch_independence(jg):
     # clips are independent: clip 1 of a batch equals the same clip run alone
     cfg = SMALL["v2-hd32"]

@@ -100,6 +100,32 @@ def test_linear(jg, dtype, epi, M, N, K):
         assert_close_16bit(got, ref, f"linear {dtype} epi {epi}")
 
 
+@pytest.mark.parametrize("epi", [1, 2, 3])
+def test_linear_split_tail_wave(jg, epi):
+    """16384 x 1024 outputs are 256 tiles of 256 x 256 for 76 resident CTA
+    pairs: three full waves, then 28 tiles split into half-width units.  Every
+    element is compared with the float64 product (K 256 keeps it quick)."""
+    M, N, K = 16384, 1024, 256
+    rng = np.random.default_rng(epi + 99)
+    A = _rounded(rng, (M, K), "bf16")
+    W = _rounded(rng, (N, K), "bf16", 0.05)
+    b = rng.standard_normal(N).astype(np.float32).astype(np.float64) * 0.1
+    resid = rng.standard_normal((M, N)).astype(np.float32).astype(np.float64)
+    out = _dev(resid) if epi == 2 else None
+    dA, dW, db = _dev(A, "bf16"), _dev(W, "bf16"), _dev(b)
+    got = jg.linear(dA, dW, db, epi, out=out).float().cpu().numpy()
+    ref = _linear_ref(A, W, b, epi, resid)
+    if epi in (1, 2):
+        m = metrics(got, ref)
+        assert m["rel_max"] <= 1e-4, (epi, m)
+    else:
+        assert_close_16bit(got, ref, "linear GELU split tail")
+    if epi != 2:
+        # one writer per output element: a second run is bit for bit the same
+        again = jg.linear(dA, dW, db, epi).float().cpu().numpy()
+        np.testing.assert_array_equal(again, got)
+
+
 def _attn_inputs(rng, B, H, N, hd, dtype, logit_std):
     # q k^T / sqrt(hd) has std ~ sq*sk*sqrt(hd)/sqrt(hd) = sq*sk
     s = math.sqrt(logit_std)

@@ -27,7 +27,7 @@ class JepaError(RuntimeError):
         self.status = status
 
 
-ABI_VERSION = 3  # JEPA_ABI_VERSION of include/jepa_gb300.h
+ABI_VERSION = 4  # JEPA_ABI_VERSION of include/jepa_gb300.h
 
 
 class EncoderParams(C.Structure):
@@ -56,6 +56,7 @@ SIGNATURES = {
     "jepa_encode_workspace_bytes": (U64, [VP, I, I, I, I]),
     "jepa_encode": (ST, [VP, VP, I, I, I, I, I, VP, VP, VP, VP]),
     "jepa_encode_host": (ST, [VP, VP, I, I, I, I, I, VP, VP, VP]),
+    "jepa_encode_host_async": (ST, [VP, VP, I, I, I, I, I, VP, VP, VP]),
     "jepa_encoder_embed": (ST, [VP, VP, I, I, I, I, I, VP, VP]),
     "jepa_encoder_blocks": (ST, [VP, VP, I, I, I, I, I, I, VP]),
     "jepa_encoder_sync": (ST, [VP, VP]),

@@ -217,6 +217,14 @@ class Encoder:
         check(self.lib.jepa_encode_host(self.handle, _ptr(clip), _lib.CLIP_U8_THWC, B, T, H, W, _ptr(out),
                                         _ptr(pooled), _stream(stream)))
 
+    def encode_host_async(self, clip: torch.Tensor, out: torch.Tensor, pooled: torch.Tensor | None = None,
+                          stream=None):
+        """Host (ideally pinned) uint8 clip in, host float out; returns at once.
+        Neither buffer may be touched until sync(stream) returns."""
+        B, T, H, W, _ = clip.shape
+        check(self.lib.jepa_encode_host_async(self.handle, _ptr(clip), _lib.CLIP_U8_THWC, B, T, H, W, _ptr(out),
+                                              _ptr(pooled), _stream(stream)))
+
     def embed(self, clip: torch.Tensor, stream=None) -> torch.Tensor:
         B, T, H, W, _ = clip.shape
         x = torch.empty((B * self.n_tokens(T, H, W), self.cfg.embed_dim), dtype=torch.float32, device=clip.device)

@@ -551,6 +551,37 @@ void record_error(const char* msg) { g_last_error = msg; }
 }  // namespace jepa
 
 // ============================================================================= encoder
+// Staging of jepa_encode_host_async: two slots used in turn, each with its
+// device clip / output buffers and the events that order its reuse; the
+// copies run on two streams of their own.
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  struct Slot {
+    void* clip = nullptr;
+    size_t clip_cap = 0;
+    void* out = nullptr;
+    size_t out_cap = 0;
+    void* pool = nullptr;
+    size_t pool_cap = 0;
+    cudaEvent_t copied_in = nullptr, encoded = nullptr, copied_out = nullptr;
+  } slot[2];
+  uint64_t calls = 0;
+  void release() {
+    for (auto& sl : slot) {
+      cudaFree(sl.clip);
+      cudaFree(sl.out);
+      cudaFree(sl.pool);
+      if (sl.copied_in) cudaEventDestroy(sl.copied_in);
+      if (sl.encoded) cudaEventDestroy(sl.encoded);
+      if (sl.copied_out) cudaEventDestroy(sl.copied_out);
+      sl = Slot{};
+    }
+    if (in) cudaStreamDestroy(in);
+    if (out) cudaStreamDestroy(out);
+    in = out = nullptr;
+  }
+};
+
 struct jepa_encoder {
   jepa_encoder_params p{};
   int device = 0, sms = 0;
@@ -574,6 +605,7 @@ struct jepa_encoder {
   size_t h_out_cap = 0;
   float* h_pool_dev = nullptr;
   size_t h_pool_cap = 0;
+  HostPipe pipe;
   GraphCache graphs;
 };
 
@@ -747,6 +779,7 @@ void jepa_encoder_destroy(jepa_encoder* enc) {
   cudaFree(enc->h_clip_dev);
   cudaFree(enc->h_out_dev);
   cudaFree(enc->h_pool_dev);
+  enc->pipe.release();
   enc->graphs.release();
   delete enc;
 }
@@ -1013,9 +1046,73 @@ jepa_status jepa_encode_host(jepa_encoder* enc, const void* host_clip, int clip_
   return read_status(enc->d_status, s);
 }
 
+jepa_status jepa_encode_host_async(jepa_encoder* enc, const void* host_clip, int clip_format, int batch,
+                                   int n_frames, int height, int width, float* host_out_tokens,
+                                   float* host_out_pooled, void* stream) {
+  Geom g;
+  JEPA_TRY(check_clip(enc, batch, n_frames, height, width, g));
+  if (host_clip == nullptr || host_out_tokens == nullptr) return fail(JEPA_ERR_ARG, "host buffers are required");
+  if (clip_format != JEPA_CLIP_U8_THWC && clip_format != JEPA_CLIP_F32_CTHW)
+    return fail(JEPA_ERR_ARG, "clip_format %d", clip_format);
+  cudaStream_t s = (cudaStream_t)stream;
+  CUDA_TRY(cudaSetDevice(enc->device));
+  HostPipe& hp = enc->pipe;
+  if (hp.in == nullptr) {
+    CUDA_TRY(cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking));
+    CUDA_TRY(cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking));
+    for (auto& sl : hp.slot) {
+      CUDA_TRY(cudaEventCreateWithFlags(&sl.copied_in, cudaEventDisableTiming));
+      CUDA_TRY(cudaEventCreateWithFlags(&sl.encoded, cudaEventDisableTiming));
+      CUDA_TRY(cudaEventCreateWithFlags(&sl.copied_out, cudaEventDisableTiming));
+    }
+  }
+  HostPipe::Slot& sl = hp.slot[hp.calls & 1];
+  const size_t px = (size_t)batch * n_frames * height * width * 3;
+  const size_t clip_bytes = clip_format == JEPA_CLIP_U8_THWC ? px : px * 4;
+  const size_t out_bytes = (size_t)batch * g.n_tok * enc->p.embed_dim * 4;
+  const size_t pool_bytes = (size_t)batch * enc->p.embed_dim * 4;
+  const size_t need[3] = {clip_bytes, out_bytes, host_out_pooled ? pool_bytes : 0};
+  void** buf[3] = {&sl.clip, &sl.out, &sl.pool};
+  size_t* cap[3] = {&sl.clip_cap, &sl.out_cap, &sl.pool_cap};
+  for (int i = 0; i < 3; ++i) {
+    if (*cap[i] >= need[i]) continue;
+    // the slot's previous encode and copy-out are done with its buffers
+    CUDA_TRY(cudaEventSynchronize(sl.encoded));
+    CUDA_TRY(cudaEventSynchronize(sl.copied_out));
+    cudaFree(*buf[i]);
+    *buf[i] = nullptr;
+    *cap[i] = 0;
+    if (cudaMalloc(buf[i], need[i]) != cudaSuccess) return fail(JEPA_ERR_OOM, "host staging slot");
+    *cap[i] = need[i];
+  }
+  // in: once the encode that last read this slot's clip is done
+  CUDA_TRY(cudaStreamWaitEvent(hp.in, sl.encoded, 0));
+  CUDA_TRY(cudaMemcpyAsync(sl.clip, host_clip, clip_bytes, cudaMemcpyHostToDevice, hp.in));
+  CUDA_TRY(cudaEventRecord(sl.copied_in, hp.in));
+  // encode: once the clip is in and the copy-out that last read this slot's output is done
+  CUDA_TRY(cudaStreamWaitEvent(s, sl.copied_in, 0));
+  CUDA_TRY(cudaStreamWaitEvent(s, sl.copied_out, 0));
+  JEPA_TRY(jepa_encode(enc, sl.clip, clip_format, batch, n_frames, height, width, (float*)sl.out,
+                       host_out_pooled ? (float*)sl.pool : nullptr, nullptr, stream));
+  CUDA_TRY(cudaEventRecord(sl.encoded, s));
+  // out: after the encode
+  CUDA_TRY(cudaStreamWaitEvent(hp.out, sl.encoded, 0));
+  CUDA_TRY(cudaMemcpyAsync(host_out_tokens, sl.out, out_bytes, cudaMemcpyDeviceToHost, hp.out));
+  if (host_out_pooled)
+    CUDA_TRY(cudaMemcpyAsync(host_out_pooled, sl.pool, pool_bytes, cudaMemcpyDeviceToHost, hp.out));
+  CUDA_TRY(cudaEventRecord(sl.copied_out, hp.out));
+  ++hp.calls;
+  return JEPA_OK;
+}
+
 jepa_status jepa_encoder_sync(jepa_encoder* enc, void* stream) {
   if (enc == nullptr) return fail(JEPA_ERR_ARG, "encoder handle is NULL");
   CUDA_TRY(cudaSetDevice(enc->device));
+  if (enc->pipe.out != nullptr) {
+    // copies of jepa_encode_host_async (the copy-out follows its encode)
+    CUDA_TRY(cudaStreamSynchronize(enc->pipe.in));
+    CUDA_TRY(cudaStreamSynchronize(enc->pipe.out));
+  }
   return read_status(enc->d_status, (cudaStream_t)stream);
 }
 
