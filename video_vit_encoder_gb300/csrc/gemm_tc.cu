@@ -80,9 +80,13 @@ __device__ __forceinline__ void stage_out_head(const EpiParams& ep, int which, u
 // has bank conflicts), and the warp then writes whole 128-byte head rows of
 // consecutive tokens, one full line per eight lanes, instead of each thread
 // writing a half sector of 32 different lines.
+//
+// n_chunks (<= BN/64) is the number of 32-column chunks this thread covers:
+// BN/64 for a whole tile, fewer for a half-width tail tile (whole heads).
 template <typename T, int BN, int HD, int LAYOUT>
 __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t taddr, int row, bool row_ok,
-                                                  int col_base, int col_off, uint8_t* stage, int M, int lane) {
+                                                  int col_base, int col_off, uint8_t* stage, int M, int lane,
+                                                  int n_chunks) {
   static_assert(HD == 32 || HD == 64, "head dim");
   static_assert((BN / 2) % HD == 0, "each half tile must hold whole heads");
   constexpr int RD = 2 * ((HD / 3) / 2);
@@ -131,6 +135,7 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
   const size_t bh0 = (size_t)clip * ep.n_head + head0;
 #pragma unroll
   for (int c = 0; c < BN / 64; ++c) {
+    if (c >= n_chunks) break;
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_wait_ld();
@@ -309,12 +314,11 @@ __device__ __forceinline__ UnitTile unit_tile(int u, int num_n, int tail_start) 
 }
 
 // Whether an instantiation's epilogue can take a half-width (BN/2) tile: each
-// epilogue warp then covers BN/4 columns, which must hold whole 128-byte
-// output blocks.  The QKV epilogue is not split: a second inlined copy of it
-// does not fit the epilogue warps' registers.
+// epilogue warp then covers BN/4 columns, which must hold whole heads (QKV)
+// or whole 128-byte output blocks.
 template <int BN, int EPI, int QHD>
 __host__ __device__ constexpr bool can_split_tail() {
-  if constexpr (EPI == EPI_QKV) return false;
+  if constexpr (EPI == EPI_QKV) return QHD > 0 && (BN / 4) % QHD == 0;
   if constexpr (EPI == EPI_RESID || EPI == EPI_F32) return (BN / 4) % 32 == 0;
   return (BN / 4) % 64 == 0;
 }
@@ -529,11 +533,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = (ut.mp * CM + rank) * kBM + row_in_tile;
       const uint32_t tlane = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN;
       uint8_t* stage_buf = sEpi + (warp - 2) * S::kEpiStage;
-      if (ut.width == BN) {
-        if constexpr (EPI == EPI_QKV) {
-          qkv_tile_epilogue<T, BN, QHD, QLAYOUT>(ep, tlane + half * (BN / 2), row, row < M, ut.col0, half * (BN / 2),
-                                                 stage_buf, M, lane);
-        } else if constexpr (EPI == EPI_RESID) {
+      if constexpr (EPI == EPI_QKV) {
+        // one code path for whole tiles and half-width tail tiles
+        const int wcols = ut.width / 2;
+        qkv_tile_epilogue<T, BN, QHD, QLAYOUT>(ep, tlane + half * wcols, row, row < M, ut.col0, half * wcols,
+                                               stage_buf, M, lane, wcols / 32);
+      } else if (ut.width == BN) {
+        if constexpr (EPI == EPI_RESID) {
           reduce_epilogue<BN / 2>(ep, &tmC, tlane + half * (BN / 2), row - lane, ut.col0 + half * (BN / 2), stage_buf,
                                   lane);
         } else {
