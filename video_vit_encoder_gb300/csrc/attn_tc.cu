@@ -1,8 +1,11 @@
 // Tensor-core attention for sm_103a, softmax(scale q k^T) v per (clip, head).
 //
-// One CTA owns two 128-row query tiles (Q0, Q1) of one (clip, head).  Keys
-// and values stream in tiles of 128 through a 4-deep TMA ring shared by both
-// query tiles.  For query tile t and key tile j:
+// A work unit is two 128-row query tiles (Q0, Q1) of one (clip, head).  CTAs
+// are persistent (one per SM) and take units in turn; keys and values stream
+// in tiles of 128 through a 4-deep TMA ring shared by both query tiles and
+// running on across units, and Q is double-buffered, so one unit's last key
+// tiles overlap the next unit's Q load and first score products.  For query
+// tile t and key tile j:
 //   S_t = Q_t K_j^T     tcgen05.mma (both operands in shared memory) into the
 //                       tile's TMEM score buffer (fp32, 128 lanes x 128 columns);
 //   softmax warpgroup t (one thread per query row) reads its row of S_t into
@@ -55,10 +58,10 @@ struct AttnSmem {
   static constexpr uint32_t kKBytes = kBKV * HD * 2;
   static constexpr uint32_t kVBytes = HD * kBKV * 2;   // two 64-key blocks of HD rows x 128 B
   static constexpr uint32_t kVBlock = HD * 128;
-  static constexpr uint32_t kOffK = 2 * kQBytes;
+  static constexpr uint32_t kOffK = 4 * kQBytes;   // two buffers of the two query tiles
   static constexpr uint32_t kOffV = kOffK + kStages * kKBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kVBytes;
-  static constexpr size_t kBytes = 1024 + kOffBar + 256;
+  static constexpr size_t kBytes = 1024 + kOffBar + 512;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -187,7 +190,7 @@ template <typename T, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, T* __restrict__ out, int n_head, int n_tok,
-                   float scale_log2, int* status) {
+                   int n_units, float scale_log2, int* status) {
   using S = AttnSmem<HD>;
   constexpr int kQKRow = HD * 2;  // bytes per Q/K row = swizzle width (128 or 64)
   extern __shared__ uint8_t smem_raw[];
@@ -196,8 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem + S::kOffK;
   uint8_t* sV = smem + S::kOffV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
-  uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
+  uint64_t* q_full = bars;                 // [2] Q buffer b loaded
+  uint64_t* q_empty = bars + 2;            // [2] Q buffer b read by both tiles' score products
+  uint64_t* kv_full = bars + 4;
   uint64_t* kv_empty = kv_full + kStages;
   uint64_t* s_full = kv_empty + kStages;  // [2] per query tile: S_t computed
   uint64_t* s_free = s_full + 2;          // [2] S_t read into registers
@@ -209,12 +213,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int q0 = blockIdx.x * (2 * kBQ);
+  // Work units: (clip x head, pair of query tiles), unit u = bh * n_qp + qp.
+  // The CTA is persistent: it takes units blockIdx.x, + gridDim.x, ...; the
+  // K/V ring, the score / P / PV barriers and the exponential tokens run on
+  // one CTA-wide key-tile counter g (unit k of the CTA, key tile j: g =
+  // k n_kv + j), so one unit's last key tiles overlap the next unit's Q load
+  // and first score products.
   const int n_kv = (n_tok + kBKV - 1) / kBKV;
+  const int n_qp = (n_tok + 2 * kBQ - 1) / (2 * kBQ);
+  const int n_my = n_units > (int)blockIdx.x ? (n_units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  const int n_g = n_my * n_kv;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 2);  // both query tiles' issuers
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 2);  // both query tiles' issuers
@@ -248,30 +262,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
-        mbar_arrive_expect_tx(q_full, 2 * S::kQBytes);
-        tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
-        tma_load_3d(sQ + S::kQBytes, &tmQ, q_full, 0, q0 + kBQ, bh);
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
-        for (int j = 0; j < n_kv; ++j) {
-          if (!mbar_wait(&kv_empty[stage], phase ^ 1)) {
-            atomicOr(status, DEV_TIMEOUT);
-            *abort_flag = 1;
+        int k = 0;
+        bool ok = true;
+        for (; ok && k < n_my; ++k) {
+          const int u = (int)blockIdx.x + k * (int)gridDim.x;
+          const int ubh = u / n_qp, uq0 = (u - ubh * n_qp) * 2 * kBQ;
+          const int qb = k & 1;
+          // Q buffer qb was last read by the score products of unit k - 2
+          if (k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) - 1) & 1)) {
+            ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&kv_full[stage], S::kKBytes + S::kVBytes);
-          tma_load_3d(sK + stage * S::kKBytes, &tmK, &kv_full[stage], 0, j * kBKV, bh);
-          tma_load_3d(sV + stage * S::kVBytes, &tmV, &kv_full[stage], j * kBKV, 0, bh);
-          tma_load_3d(sV + stage * S::kVBytes + S::kVBlock, &tmV, &kv_full[stage], j * kBKV + 64, 0, bh);
-          ++issued;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
+          mbar_arrive_expect_tx(&q_full[qb], 2 * S::kQBytes);
+          tma_load_3d(sQ + qb * 2 * S::kQBytes, &tmQ, &q_full[qb], 0, uq0, ubh);
+          tma_load_3d(sQ + qb * 2 * S::kQBytes + S::kQBytes, &tmQ, &q_full[qb], 0, uq0 + kBQ, ubh);
+          for (int j = 0; j < n_kv; ++j) {
+            if (*abort_flag || !mbar_wait(&kv_empty[stage], phase ^ 1)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&kv_full[stage], S::kKBytes + S::kVBytes);
+            tma_load_3d(sK + stage * S::kKBytes, &tmK, &kv_full[stage], 0, j * kBKV, ubh);
+            tma_load_3d(sV + stage * S::kVBytes, &tmV, &kv_full[stage], j * kBKV, 0, ubh);
+            tma_load_3d(sV + stage * S::kVBytes + S::kVBlock, &tmV, &kv_full[stage], j * kBKV + 64, 0, ubh);
+            ++issued;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
-        // the CTA does not exit with copies in flight
-        mbar_wait(q_full, 0);
+        if (!ok) {
+          atomicOr(status, DEV_TIMEOUT);
+          *abort_flag = 1;
+        }
+        // The CTA does not exit with copies in flight: the last (up to two) Q
+        // loads and the last min(issued, kStages) K/V stages have landed.
+        for (int kk = k - 1; kk >= 0 && kk >= k - 2; --kk) mbar_wait(&q_full[kk & 1], (kk >> 1) & 1);
         const int pending = issued < kStages ? issued : kStages;
         for (int i = 0; i < pending; ++i) {
           if (--stage < 0) {
@@ -288,44 +318,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = warp - 1;
       constexpr uint32_t idesc_s = idesc_f16<T, kBQ, kBKV>();
       constexpr uint32_t idesc_o = idesc_f16<T, kBQ, HD>();
-      const uint64_t dq = smem_desc_kmajor<kQKRow>(smem_u32(sQ + t * S::kQBytes));
       const uint32_t dS = tmem + kColS + t * kBKV, dP = tmem + kColP + t * 64, dO = tmem + kColO + t * 64;
-      bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0));
-      // S_t of key tile j into the tile's score buffer, once the tile's
-      // softmax has read the previous scores out of it.
-      auto issue_s = [&](int j) -> bool {
-        const int stage = j % kStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[stage], (j / kStages) & 1))) return false;
-        if (j >= 1 && !__all_sync(0xffffffffu, mbar_wait(&s_free[t], (j - 1) & 1))) return false;
+      bool ok = true;
+      // S_t of the next CTA key tile (unit ks, key tile js, ring stage
+      // st_s) into the tile's score buffer, once the tile's softmax has read
+      // the previous scores out of it (and, for a unit's first key tile, once
+      // its Q has landed).  Counters advance without divisions.
+      int gs = 0, ks = 0, js = 0, st_s = 0;
+      uint32_t ph_s = 0;
+      auto issue_s = [&]() -> bool {
+        if (js == 0 && !__all_sync(0xffffffffu, mbar_wait(&q_full[ks & 1], (ks >> 1) & 1))) return false;
+        if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[st_s], ph_s))) return false;
+        if (gs >= 1 && !__all_sync(0xffffffffu, mbar_wait(&s_free[t], (gs - 1) & 1))) return false;
         tc_fence_after();
-        const uint64_t dk = smem_desc_kmajor<kQKRow>(smem_u32(sK + stage * S::kKBytes));
+        const uint64_t dq = smem_desc_kmajor<kQKRow>(smem_u32(sQ + (ks & 1) * 2 * S::kQBytes + t * S::kQBytes));
+        const uint64_t dk = smem_desc_kmajor<kQKRow>(smem_u32(sK + st_s * S::kKBytes));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)  // +32 bytes along K = +2 in the descriptor's address field
           umma_f16_ss_warp(dS, dq + kk * 2, dk + kk * 2, idesc_s, kk != 0);
         umma_commit_warp(&s_full[t]);
+        if (js == n_kv - 1) umma_commit_warp(&q_empty[ks & 1]);  // this tile is done with the unit's Q
+        ++gs;
+        if (++js == n_kv) {
+          js = 0;
+          ++ks;
+        }
+        if (++st_s == kStages) {
+          st_s = 0;
+          ph_s ^= 1;
+        }
         return true;
       };
-      // O_t += P_t V_j, P_t from tensor memory (8 columns per 16 keys).
-      auto issue_pv = [&](int j) -> bool {
-        if (!__all_sync(0xffffffffu, mbar_wait(&p_full[t], j & 1))) return false;
+      // O_t += P_t V of the next CTA key tile, P_t from tensor memory (8
+      // columns per 16 keys); a unit's first key tile starts O_t afresh.  The
+      // softmax signals P only after it has read the previous unit's O_t.
+      int gp = 0, jp = 0, st_p = 0;
+      auto issue_pv = [&]() -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait(&p_full[t], gp & 1))) return false;
         tc_fence_after();
-        const int stage = j % kStages;
-        const uint64_t dv = smem_desc_kmajor<128>(smem_u32(sV + stage * S::kVBytes));
+        const uint64_t dv = smem_desc_kmajor<128>(smem_u32(sV + st_p * S::kVBytes));
 #pragma unroll
         for (int kk = 0; kk < kBKV / 16; ++kk)
           umma_f16_ts_warp(dO, dP + kk * 8, dv + (kk >> 2) * (S::kVBlock >> 4) + (kk & 3) * 2, idesc_o,
-                           (j | kk) != 0);
+                           (jp | kk) != 0);
         umma_commit_warp(&pv_done[t]);
-        umma_commit_warp(&kv_empty[stage]);  // this tile is done with K_j and V_j
+        umma_commit_warp(&kv_empty[st_p]);  // this tile is done with this key tile's K and V
+        ++gp;
+        if (++jp == n_kv) jp = 0;
+        if (++st_p == kStages) st_p = 0;
         return true;
       };
-      // Order: S_0, then per key tile j: S_{j+1}, PV_j, so the next scores
-      // are queued before PV_j waits for the softmax.
-      ok = ok && issue_s(0);
-      for (int j = 0; ok && j < n_kv; ++j) {
+      // Order: S_0, then per key tile g: S_{g+1}, PV_g, so the next scores
+      // (possibly the next unit's first) are queued before PV_g waits for the softmax.
+      if (n_g > 0) ok = issue_s();
+      for (int g = 0; ok && g < n_g; ++g) {
         if (__any_sync(0xffffffffu, *abort_flag)) break;
-        if (j + 1 < n_kv) ok = issue_s(j + 1);
-        ok = ok && issue_pv(j);
+        if (g + 1 < n_g) ok = issue_s();
+        ok = ok && issue_pv();
       }
       if (!ok && lane == 0) {
         atomicOr(status, DEV_TIMEOUT);
@@ -343,94 +392,107 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + kColS + t * kBKV;
     const uint32_t tP = tmem + lane_off + kColP + t * 64;
     const uint32_t tO = tmem + lane_off + kColO + t * 64;
-    float m = -INFINITY;  // running max of the raw scores
-    float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const bool w_ok = mbar_wait(&s_full[t], j & 1);
-      // tcgen05.ld/st are warp-collective: every decision that guards them is warp-uniform.
-      if (__any_sync(0xffffffffu, !w_ok || *abort_flag)) {
+    int g = 0;  // the CTA's key-tile counter over its units
+    for (int k = 0; ok && k < n_my; ++k) {
+      const int u = (int)blockIdx.x + k * (int)gridDim.x;
+      const int ubh = u / n_qp, uq0 = (u - ubh * n_qp) * 2 * kBQ;
+      float m = -INFINITY;  // running max of the raw scores
+      float l = 0.f;
+      for (int j = 0; j < n_kv; ++j, ++g) {
+        const bool w_ok = mbar_wait(&s_full[t], g & 1);
+        // tcgen05.ld/st are warp-collective: every decision that guards them is warp-uniform.
+        if (__any_sync(0xffffffffu, !w_ok || *abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // the whole score row into registers in one TMEM round trip; the
+        // buffer is released at once so the next scores can be computed into it
+        uint32_t sv[kBKV / 32][32];
+#pragma unroll
+        for (int c = 0; c < kBKV / 32; ++c) tmem_ld32(tS + c * 32, sv[c]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&s_free[t]);
+        const int kvalid = n_tok - j * kBKV;   // keys of this tile inside the sequence
+        const bool full_tile = kvalid >= kBKV;
+        const float mx = full_tile ? row_max<false>(sv, kvalid) : row_max<true>(sv, kvalid);
+        if (j == 0) m = mx;
+        // O_t is stable and P_t's buffer free once PV_t of the previous key
+        // tile is done (for a unit's first key tile that wait came before the
+        // previous unit's output).
+        if (j >= 1 && !mbar_wait(&pv_done[t], (g - 1) & 1)) ok = false;
+        tc_fence_after();
+        // Move the running max of the warp's rows when any grew by more than 2^8
+        // (in the exponent): O_t and l are rescaled by 2^((m_old - m_new) scale log2e).
+        if (__any_sync(0xffffffffu, j > 0 && (mx - m) * scale_log2 > 8.0f)) {
+          const float m_new = fmaxf(m, mx);
+          const float corr = ex2((m - m_new) * scale_log2);
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t uo[32];
+            tmem_ld32(tO + c * 32, uo);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) uo[i] = __float_as_uint(__uint_as_float(uo[i]) * corr);
+            tmem_st32(tO + c * 32, uo);
+          }
+          l *= corr;
+          m = m_new;
+        }
+        // The two tiles' warps on one SM sub-partition take turns at the
+        // exponentials (Q0 of key tile g, Q1 of g, Q0 of g+1, ...), so one
+        // tile's TMEM load and row max overlap the other's special-function
+        // work instead of both contending for it at once.
+        if (t == 1 || g >= 1) {
+          const bool tok_ok = mbar_wait(&exp_tok[(1 - t) * 4 + quarter], (t == 0 ? g - 1 : g) & 1);
+          if (!tok_ok) ok = false;
+        }
+        // P = 2^((S - m) scale log2e), 16-bit, into tensor memory
+        const float rs = full_tile ? exp_to_tmem<T, false>(sv, kvalid, scale_log2, -m * scale_log2, tP)
+                                   : exp_to_tmem<T, true>(sv, kvalid, scale_log2, -m * scale_log2, tP);
+        l += rs;
+        mbar_arrive(&exp_tok[t * 4 + quarter]);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
+        if (__any_sync(0xffffffffu, !ok)) break;
+      }
+      // the unit's last PV (its commit follows every earlier MMA of the issuer)
+      if (ok) ok = mbar_wait(&pv_done[t], (g - 1) & 1);
+      if (__any_sync(0xffffffffu, !ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // the whole score row into registers in one TMEM round trip; the
-      // buffer is released at once so the next scores can be computed into it
-      uint32_t sv[kBKV / 32][32];
-#pragma unroll
-      for (int c = 0; c < kBKV / 32; ++c) tmem_ld32(tS + c * 32, sv[c]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s_free[t]);
-      const int kvalid = n_tok - j * kBKV;   // keys of this tile inside the sequence
-      const bool full_tile = kvalid >= kBKV;
-      const float mx = full_tile ? row_max<false>(sv, kvalid) : row_max<true>(sv, kvalid);
-      if (j == 0) m = mx;
-      // O_t is stable and P_t's buffer free once PV_t of the previous key tile is done.
-      if (j >= 1 && !mbar_wait(&pv_done[t], (j - 1) & 1)) ok = false;
-      tc_fence_after();
-      // Move the running max of the warp's rows when any grew by more than 2^8
-      // (in the exponent): O_t and l are rescaled by 2^((m_old - m_new) scale log2e).
-      if (__any_sync(0xffffffffu, j > 0 && (mx - m) * scale_log2 > 8.0f)) {
-        const float m_new = fmaxf(m, mx);
-        const float corr = ex2((m - m_new) * scale_log2);
-#pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tO + c * 32, u);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * corr);
-          tmem_st32(tO + c * 32, u);
-        }
-        l *= corr;
-        m = m_new;
-      }
-      // The two tiles' warps on one SM sub-partition take turns at the
-      // exponentials (Q0 of key tile j, Q1 of j, Q0 of j+1, ...), so one
-      // tile's TMEM load and row max overlap the other's special-function
-      // work instead of both contending for it at once.
-      if (t == 1 || j >= 1) {
-        const bool tok_ok = mbar_wait(&exp_tok[(1 - t) * 4 + quarter], (t == 0 ? j - 1 : j) & 1);
-        if (!tok_ok) ok = false;
-      }
-      // P = 2^((S - m) scale log2e), 16-bit, into tensor memory
-      const float rs = full_tile ? exp_to_tmem<T, false>(sv, kvalid, scale_log2, -m * scale_log2, tP)
-                                 : exp_to_tmem<T, true>(sv, kvalid, scale_log2, -m * scale_log2, tP);
-      l += rs;
-      mbar_arrive(&exp_tok[t * 4 + quarter]);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&p_full[t]);
-      if (__any_sync(0xffffffffu, !ok)) break;
-    }
-    if (ok) ok = mbar_wait(&pv_done[t], (n_kv - 1) & 1);
-    if (__any_sync(0xffffffffu, !ok)) {
-      if (lane == 0) atomicOr(status, DEV_TIMEOUT);
-      *abort_flag = 1;
-    } else {
-      tc_fence_after();
-      const int row = q0 + t * kBQ + quarter * 32 + lane;
+      const int row = uq0 + t * kBQ + quarter * 32 + lane;
       const float inv = 1.0f / l;
-      const int b = bh / n_head, head = bh - (bh / n_head) * n_head;
+      const int b = ubh / n_head, head = ubh - (ubh / n_head) * n_head;
       T* op = out + ((size_t)b * n_tok + row) * (size_t)(n_head * HD) + head * HD;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tO + c * 32, u);
+        uint32_t uo[32];
+        tmem_ld32(tO + c * 32, uo);
         tmem_wait_ld();
         if (row < n_tok) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint4 w;
-            w.x = pack2<T>(__uint_as_float(u[8 * i + 0]) * inv, __uint_as_float(u[8 * i + 1]) * inv);
-            w.y = pack2<T>(__uint_as_float(u[8 * i + 2]) * inv, __uint_as_float(u[8 * i + 3]) * inv);
-            w.z = pack2<T>(__uint_as_float(u[8 * i + 4]) * inv, __uint_as_float(u[8 * i + 5]) * inv);
-            w.w = pack2<T>(__uint_as_float(u[8 * i + 6]) * inv, __uint_as_float(u[8 * i + 7]) * inv);
+            w.x = pack2<T>(__uint_as_float(uo[8 * i + 0]) * inv, __uint_as_float(uo[8 * i + 1]) * inv);
+            w.y = pack2<T>(__uint_as_float(uo[8 * i + 2]) * inv, __uint_as_float(uo[8 * i + 3]) * inv);
+            w.z = pack2<T>(__uint_as_float(uo[8 * i + 4]) * inv, __uint_as_float(uo[8 * i + 5]) * inv);
+            w.w = pack2<T>(__uint_as_float(uo[8 * i + 6]) * inv, __uint_as_float(uo[8 * i + 7]) * inv);
             reinterpret_cast<uint4*>(op + c * 32)[i] = w;
           }
         }
       }
+      // The next unit's first P (and so its first PV, which starts O_t afresh)
+      // is signalled after these reads, behind the same fence.
+    }
+    if (!ok) {
+      if (lane == 0) atomicOr(status, DEV_TIMEOUT);
+      *abort_flag = 1;
     }
   }
 
@@ -444,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <typename T, int HD>
 cudaError_t launch_t(const void* q, const void* k, const void* vt, void* out, int batch, int n_head, int n_tok,
-                     int ldv, float scale, int* status, cudaStream_t s) {
+                     int ldv, float scale, int* status, cudaStream_t s, int num_sms) {
   using S = AttnSmem<HD>;
   const uint64_t BH = (uint64_t)batch * n_head;
   CUtensorMap tq, tk, tv;
@@ -467,8 +529,13 @@ cudaError_t launch_t(const void* q, const void* k, const void* vt, void* out, in
     if (fa.numRegs * kThreads < 128 * kRegsControl + 256 * kRegsSoftmax) return cudaErrorInvalidConfiguration;
     configured = true;
   }
-  dim3 grid((n_tok + 2 * kBQ - 1) / (2 * kBQ), (unsigned)BH);
-  kern<<<grid, kThreads, S::kBytes, s>>>(tq, tk, tv, (T*)out, n_head, n_tok, scale * 1.4426950408889634f, status);
+  // persistent grid: one CTA per SM (its shared memory allows no second), each
+  // taking every gridDim-th unit
+  const int n_units = (int)(((n_tok + 2 * kBQ - 1) / (2 * kBQ)) * BH);
+  const int slots = num_sms > 0 ? num_sms : 1;
+  const int grid = n_units < slots ? n_units : slots;
+  kern<<<grid, kThreads, S::kBytes, s>>>(tq, tk, tv, (T*)out, n_head, n_tok, n_units, scale * 1.4426950408889634f,
+                                         status);
   return cudaGetLastError();
 }
 
@@ -476,13 +543,12 @@ cudaError_t launch_t(const void* q, const void* k, const void* vt, void* out, in
 
 cudaError_t attention_tc(int dtype, const void* q, const void* k, const void* vt, void* out, int batch, int n_head,
                          int n_tok, int head_dim, int ldv, float scale, int* status, cudaStream_t s, int num_sms) {
-  (void)num_sms;
   if (dtype == DTYPE_BF16) {
-    if (head_dim == 64) return launch_t<__nv_bfloat16, 64>(q, k, vt, out, batch, n_head, n_tok, ldv, scale, status, s);
-    if (head_dim == 32) return launch_t<__nv_bfloat16, 32>(q, k, vt, out, batch, n_head, n_tok, ldv, scale, status, s);
+    if (head_dim == 64) return launch_t<__nv_bfloat16, 64>(q, k, vt, out, batch, n_head, n_tok, ldv, scale, status, s, num_sms);
+    if (head_dim == 32) return launch_t<__nv_bfloat16, 32>(q, k, vt, out, batch, n_head, n_tok, ldv, scale, status, s, num_sms);
   } else if (dtype == DTYPE_F16) {
-    if (head_dim == 64) return launch_t<__half, 64>(q, k, vt, out, batch, n_head, n_tok, ldv, scale, status, s);
-    if (head_dim == 32) return launch_t<__half, 32>(q, k, vt, out, batch, n_head, n_tok, ldv, scale, status, s);
+    if (head_dim == 64) return launch_t<__half, 64>(q, k, vt, out, batch, n_head, n_tok, ldv, scale, status, s, num_sms);
+    if (head_dim == 32) return launch_t<__half, 32>(q, k, vt, out, batch, n_head, n_tok, ldv, scale, status, s, num_sms);
   }
   return cudaErrorInvalidValue;
 }
