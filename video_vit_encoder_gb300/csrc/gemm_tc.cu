@@ -6,7 +6,9 @@
 // warps drain the accumulator with tcgen05.ld and apply the fused epilogue.
 // The kernel is persistent (one CTA per SM, static tile striding) and keeps
 // two accumulators in tensor memory so the epilogue of one tile overlaps the
-// main loop of the next.
+// main loop of the next.  The tiles of the last, partial wave are split into
+// two half-width units run by different CTAs, so that wave takes about half
+// a tile's time instead of a whole one.
 //
 // Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and
 // tensor-memory owner, warps 2-9 epilogue (warp w reads TMEM lanes
