@@ -162,6 +162,23 @@ def test_attention_tc(jg, dtype, hd, N, logit_std):
     assert_close_16bit(got, ref, f"attention {dtype} hd{hd} N{N}")
 
 
+@pytest.mark.parametrize("N", [300, 384])
+def test_attention_tc_many_units_per_cta(jg, N):
+    """8 clips x 16 heads give 256 units of two query tiles, more than there
+    are SMs, so persistent CTAs run two units each; 3 key tiles per unit (an
+    odd count, so the CTA-wide barrier parities flip mid-unit) and, at N 300,
+    a ragged last key tile and a half-empty second query tile.  Planted large
+    logits move the running max in the first and in the last key tile."""
+    B, H, hd, dtype = 8, 16, 64, "bf16"
+    rng = np.random.default_rng(N + 17)
+    q, k, v = _attn_inputs(rng, B, H, N, hd, dtype, 4.0)
+    k[:, 7] = synth.round_to_dtype(q[:, 3] * 3, dtype)
+    k[:, N - 5] = synth.round_to_dtype(q[:, 130] * 3, dtype)
+    got = _run_attn(jg, q, k, v, B, H, N, hd, dtype)
+    ref = oracle.attention_heads(q, k, v).reshape(B, H, N, hd).transpose(0, 2, 1, 3).reshape(B, N, H * hd)
+    assert_close_16bit(got, ref, f"attention many units N{N}")
+
+
 @pytest.mark.parametrize("N,hd", [(2048, 64), (8192, 64), (8192, 32), (18432, 64)])
 @pytest.mark.parametrize("logit_std", [1.0, 4.0])
 def test_attention_tc_long_sampled_rows(jg, N, hd, logit_std):
