@@ -264,10 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         int stage = 0;
         uint32_t phase = 0;
-        int issued = 0;
-        int k = 0;
+        int issued = 0;    // K/V stage loads
+        int q_issued = 0;  // Q loads (one per unit)
         bool ok = true;
-        for (; ok && k < n_my; ++k) {
+        for (int k = 0; ok && k < n_my; ++k) {
           const int u = (int)blockIdx.x + k * (int)gridDim.x;
           const int ubh = u / n_qp, uq0 = (u - ubh * n_qp) * 2 * kBQ;
           const int qb = k & 1;
@@ -279,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&q_full[qb], 2 * S::kQBytes);
           tma_load_3d(sQ + qb * 2 * S::kQBytes, &tmQ, &q_full[qb], 0, uq0, ubh);
           tma_load_3d(sQ + qb * 2 * S::kQBytes + S::kQBytes, &tmQ, &q_full[qb], 0, uq0 + kBQ, ubh);
+          ++q_issued;
           for (int j = 0; j < n_kv; ++j) {
             if (*abort_flag || !mbar_wait(&kv_empty[stage], phase ^ 1)) {
               ok = false;
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // The CTA does not exit with copies in flight: the last (up to two) Q
         // loads and the last min(issued, kStages) K/V stages have landed.
-        for (int kk = k - 1; kk >= 0 && kk >= k - 2; --kk) mbar_wait(&q_full[kk & 1], (kk >> 1) & 1);
+        for (int kk = q_issued - 1; kk >= 0 && kk >= q_issued - 2; --kk) mbar_wait(&q_full[kk & 1], (kk >> 1) & 1);
         const int pending = issued < kStages ? issued : kStages;
         for (int i = 0; i < pending; ++i) {
           if (--stage < 0) {
