@@ -1,11 +1,12 @@
 // Tensor-core attention for sm_103a, softmax(scale q k^T) v per (clip, head).
 //
-// A work unit is two 128-row query tiles (Q0, Q1) of one (clip, head).  CTAs
-// are persistent (one per SM) and take units in turn; keys and values stream
-// in tiles of 128 through a 4-deep TMA ring shared by both query tiles and
-// running on across units, and Q is double-buffered, so one unit's last key
-// tiles overlap the next unit's Q load and first score products.  For query
-// tile t and key tile j:
+// A work unit is two 128-row query tiles (Q0, Q1) of one (clip, head); keys
+// and values stream in tiles of 128 through a 4-deep TMA ring shared by both
+// query tiles.  Two launch forms: for short sequences the CTAs are persistent
+// (one per SM, taking units in turn, the ring running on across units and Q
+// double-buffered, so one unit's last key tiles overlap the next unit's Q
+// load and first score products); for longer ones each CTA takes one unit on
+// a grid over the units.  For query tile t and key tile j:
 //   S_t = Q_t K_j^T     tcgen05.mma (both operands in shared memory) into the
 //                       tile's TMEM score buffer (fp32, 128 lanes x 128 columns);
 //   softmax warpgroup t (one thread per query row) reads its row of S_t into
@@ -52,13 +53,13 @@ constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
 // polynomial and the rest by ex2.approx (balances the two pipes).
 constexpr int kPolyPairs = 0;
 
-template <int HD>
+template <int HD, int QBUF>
 struct AttnSmem {
   static constexpr uint32_t kQBytes = kBQ * HD * 2;    // one query tile
   static constexpr uint32_t kKBytes = kBKV * HD * 2;
   static constexpr uint32_t kVBytes = HD * kBKV * 2;   // two 64-key blocks of HD rows x 128 B
   static constexpr uint32_t kVBlock = HD * 128;
-  static constexpr uint32_t kOffK = 4 * kQBytes;   // two buffers of the two query tiles
+  static constexpr uint32_t kOffK = 2 * QBUF * kQBytes;   // QBUF buffers of the two query tiles
   static constexpr uint32_t kOffV = kOffK + kStages * kKBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kVBytes;
   static constexpr size_t kBytes = 1024 + kOffBar + 512;
@@ -186,12 +187,275 @@ __device__ __forceinline__ float exp_to_tmem(const uint32_t (&s)[kBKV / 32][32],
   return a + b;
 }
 
+// One unit (two query tiles of one (clip, head)) per CTA, on a grid over
+// the units: the hardware hands each SM its next CTA as one finishes.
 template <typename T, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, T* __restrict__ out, int n_head, int n_tok,
-                   int n_units, float scale_log2, int* status) {
-  using S = AttnSmem<HD>;
+                   float scale_log2, int* status) {
+  using S = AttnSmem<HD, 1>;
+  constexpr int kQKRow = HD * 2;  // bytes per Q/K row = swizzle width (128 or 64)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + S::kOffK;
+  uint8_t* sV = smem + S::kOffV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + kStages;
+  uint64_t* s_full = kv_empty + kStages;  // [2] per query tile: S_t computed
+  uint64_t* s_free = s_full + 2;          // [2] S_t read into registers
+  uint64_t* p_full = s_free + 2;          // [2] P_t written (and O_t rescaled)
+  uint64_t* pv_done = p_full + 2;         // [2] O_t += P_t V done
+  uint64_t* mma_done = pv_done + 2;      // [2] per issuer
+  uint64_t* exp_tok = mma_done + 2;      // [2][4] exponential phase of tile t done, per TMEM quarter
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(exp_tok + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y;
+  const int q0 = blockIdx.x * (2 * kBQ);
+  const int n_kv = (n_tok + kBKV - 1) / kBKV;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 2);  // both query tiles' issuers
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&exp_tok[i], 32);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_full, 2 * S::kQBytes);
+        tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
+        tma_load_3d(sQ + S::kQBytes, &tmQ, q_full, 0, q0 + kBQ, bh);
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        for (int j = 0; j < n_kv; ++j) {
+          if (!mbar_wait(&kv_empty[stage], phase ^ 1)) {
+            atomicOr(status, DEV_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[stage], S::kKBytes + S::kVBytes);
+          tma_load_3d(sK + stage * S::kKBytes, &tmK, &kv_full[stage], 0, j * kBKV, bh);
+          tma_load_3d(sV + stage * S::kVBytes, &tmV, &kv_full[stage], j * kBKV, 0, bh);
+          tma_load_3d(sV + stage * S::kVBytes + S::kVBlock, &tmV, &kv_full[stage], j * kBKV + 64, 0, bh);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        // the CTA does not exit with copies in flight
+        mbar_wait(q_full, 0);
+        const int pending = issued < kStages ? issued : kStages;
+        for (int i = 0; i < pending; ++i) {
+          if (--stage < 0) {
+            stage = kStages - 1;
+            phase ^= 1;
+          }
+          mbar_wait(&kv_full[stage], phase);
+        }
+      }
+    } else if (warp == 1 || warp == 2) {
+      // ------------------------------------------------------------ MMA issuer of query tile t
+      // The whole warp walks the schedule (waits are warp-uniform); one
+      // elected lane issues each MMA and commit.
+      const int t = warp - 1;
+      constexpr uint32_t idesc_s = idesc_f16<T, kBQ, kBKV>();
+      constexpr uint32_t idesc_o = idesc_f16<T, kBQ, HD>();
+      const uint64_t dq = smem_desc_kmajor<kQKRow>(smem_u32(sQ + t * S::kQBytes));
+      const uint32_t dS = tmem + kColS + t * kBKV, dP = tmem + kColP + t * 64, dO = tmem + kColO + t * 64;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0));
+      // S_t of key tile j into the tile's score buffer, once the tile's
+      // softmax has read the previous scores out of it.
+      auto issue_s = [&](int j) -> bool {
+        const int stage = j % kStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[stage], (j / kStages) & 1))) return false;
+        if (j >= 1 && !__all_sync(0xffffffffu, mbar_wait(&s_free[t], (j - 1) & 1))) return false;
+        tc_fence_after();
+        const uint64_t dk = smem_desc_kmajor<kQKRow>(smem_u32(sK + stage * S::kKBytes));
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)  // +32 bytes along K = +2 in the descriptor's address field
+          umma_f16_ss_warp(dS, dq + kk * 2, dk + kk * 2, idesc_s, kk != 0);
+        umma_commit_warp(&s_full[t]);
+        return true;
+      };
+      // O_t += P_t V_j, P_t from tensor memory (8 columns per 16 keys).
+      auto issue_pv = [&](int j) -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait(&p_full[t], j & 1))) return false;
+        tc_fence_after();
+        const int stage = j % kStages;
+        const uint64_t dv = smem_desc_kmajor<128>(smem_u32(sV + stage * S::kVBytes));
+#pragma unroll
+        for (int kk = 0; kk < kBKV / 16; ++kk)
+          umma_f16_ts_warp(dO, dP + kk * 8, dv + (kk >> 2) * (S::kVBlock >> 4) + (kk & 3) * 2, idesc_o,
+                           (j | kk) != 0);
+        umma_commit_warp(&pv_done[t]);
+        umma_commit_warp(&kv_empty[stage]);  // this tile is done with K_j and V_j
+        return true;
+      };
+      // Order: S_0, then per key tile j: S_{j+1}, PV_j, so the next scores
+      // are queued before PV_j waits for the softmax.
+      ok = ok && issue_s(0);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (__any_sync(0xffffffffu, *abort_flag)) break;
+        if (j + 1 < n_kv) ok = issue_s(j + 1);
+        ok = ok && issue_pv(j);
+      }
+      if (!ok && lane == 0) {
+        atomicOr(status, DEV_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit_warp(&mma_done[t]);
+      mbar_wait(&mma_done[t], 0);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    // ------------------------------------------------------------ softmax + output (tile t)
+    const int t = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + kColS + t * kBKV;
+    const uint32_t tP = tmem + lane_off + kColP + t * 64;
+    const uint32_t tO = tmem + lane_off + kColO + t * 64;
+    float m = -INFINITY;  // running max of the raw scores
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const bool w_ok = mbar_wait(&s_full[t], j & 1);
+      // tcgen05.ld/st are warp-collective: every decision that guards them is warp-uniform.
+      if (__any_sync(0xffffffffu, !w_ok || *abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // the whole score row into registers in one TMEM round trip; the
+      // buffer is released at once so the next scores can be computed into it
+      uint32_t sv[kBKV / 32][32];
+#pragma unroll
+      for (int c = 0; c < kBKV / 32; ++c) tmem_ld32(tS + c * 32, sv[c]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s_free[t]);
+      const int kvalid = n_tok - j * kBKV;   // keys of this tile inside the sequence
+      const bool full_tile = kvalid >= kBKV;
+      const float mx = full_tile ? row_max<false>(sv, kvalid) : row_max<true>(sv, kvalid);
+      if (j == 0) m = mx;
+      // O_t is stable and P_t's buffer free once PV_t of the previous key tile is done.
+      if (j >= 1 && !mbar_wait(&pv_done[t], (j - 1) & 1)) ok = false;
+      tc_fence_after();
+      // Move the running max of the warp's rows when any grew by more than 2^8
+      // (in the exponent): O_t and l are rescaled by 2^((m_old - m_new) scale log2e).
+      if (__any_sync(0xffffffffu, j > 0 && (mx - m) * scale_log2 > 8.0f)) {
+        const float m_new = fmaxf(m, mx);
+        const float corr = ex2((m - m_new) * scale_log2);
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tO + c * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * corr);
+          tmem_st32(tO + c * 32, u);
+        }
+        l *= corr;
+        m = m_new;
+      }
+      // The two tiles' warps on one SM sub-partition take turns at the
+      // exponentials (Q0 of key tile j, Q1 of j, Q0 of j+1, ...), so one
+      // tile's TMEM load and row max overlap the other's special-function
+      // work instead of both contending for it at once.
+      if (t == 1 || j >= 1) {
+        const bool tok_ok = mbar_wait(&exp_tok[(1 - t) * 4 + quarter], (t == 0 ? j - 1 : j) & 1);
+        if (!tok_ok) ok = false;
+      }
+      // P = 2^((S - m) scale log2e), 16-bit, into tensor memory
+      const float rs = full_tile ? exp_to_tmem<T, false>(sv, kvalid, scale_log2, -m * scale_log2, tP)
+                                 : exp_to_tmem<T, true>(sv, kvalid, scale_log2, -m * scale_log2, tP);
+      l += rs;
+      mbar_arrive(&exp_tok[t * 4 + quarter]);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full[t]);
+      if (__any_sync(0xffffffffu, !ok)) break;
+    }
+    if (ok) ok = mbar_wait(&pv_done[t], (n_kv - 1) & 1);
+    if (__any_sync(0xffffffffu, !ok)) {
+      if (lane == 0) atomicOr(status, DEV_TIMEOUT);
+      *abort_flag = 1;
+    } else {
+      tc_fence_after();
+      const int row = q0 + t * kBQ + quarter * 32 + lane;
+      const float inv = 1.0f / l;
+      const int b = bh / n_head, head = bh - (bh / n_head) * n_head;
+      T* op = out + ((size_t)b * n_tok + row) * (size_t)(n_head * HD) + head * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tO + c * 32, u);
+        tmem_wait_ld();
+        if (row < n_tok) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack2<T>(__uint_as_float(u[8 * i + 0]) * inv, __uint_as_float(u[8 * i + 1]) * inv);
+            w.y = pack2<T>(__uint_as_float(u[8 * i + 2]) * inv, __uint_as_float(u[8 * i + 3]) * inv);
+            w.z = pack2<T>(__uint_as_float(u[8 * i + 4]) * inv, __uint_as_float(u[8 * i + 5]) * inv);
+            w.w = pack2<T>(__uint_as_float(u[8 * i + 6]) * inv, __uint_as_float(u[8 * i + 7]) * inv);
+            reinterpret_cast<uint4*>(op + c * 32)[i] = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// The same computation with persistent CTAs (described at the top of the
+// file): one per SM, taking units in turn.
+template <typename T, int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                              const __grid_constant__ CUtensorMap tmV, T* __restrict__ out, int n_head, int n_tok,
+                              int n_units, float scale_log2, int* status) {
+  using S = AttnSmem<HD, 2>;
   constexpr int kQKRow = HD * 2;  // bytes per Q/K row = swizzle width (128 or 64)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -505,10 +769,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Sequences of at most this many key tiles run on the persistent kernel:
+// there each unit is short, and overlapping its start with the previous
+// unit's end pays (576-token images: 1.06 -> 0.92 ms per step).  Longer units
+// run one per CTA: the hardware's dynamic hand-out of CTAs balances them
+// better than a fixed round-robin (8192 and 18432 tokens: 9-10 % faster).
+constexpr int kPersistentMaxKeyTiles = 8;
+
+template <typename Kern>
+cudaError_t configure(Kern kern, size_t smem_bytes) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+  if (e != cudaSuccess) return e;
+  // setmaxnreg.inc waits until the registers it asks for are free within the
+  // block's launch allocation: refuse to launch when the allocation is short.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * kThreads < 128 * kRegsControl + 256 * kRegsSoftmax) return cudaErrorInvalidConfiguration;
+  return cudaSuccess;
+}
+
 template <typename T, int HD>
 cudaError_t launch_t(const void* q, const void* k, const void* vt, void* out, int batch, int n_head, int n_tok,
                      int ldv, float scale, int* status, cudaStream_t s, int num_sms) {
-  using S = AttnSmem<HD>;
   const uint64_t BH = (uint64_t)batch * n_head;
   CUtensorMap tq, tk, tv;
   cudaError_t e = make_tmap_3d(&tq, q, 2, HD, n_tok, BH, (uint64_t)HD * 2, (uint64_t)n_tok * HD * 2, HD, kBQ, 1);
@@ -517,26 +800,36 @@ cudaError_t launch_t(const void* q, const void* k, const void* vt, void* out, in
   if (e != cudaSuccess) return e;
   e = make_tmap_3d(&tv, vt, 2, n_tok, HD, BH, (uint64_t)ldv * 2, (uint64_t)ldv * HD * 2, 64, HD, 1);
   if (e != cudaSuccess) return e;
-  auto kern = attn_tc_kernel<T, HD>;
+  const float scale_log2 = scale * 1.4426950408889634f;
+  const int n_qp = (n_tok + 2 * kBQ - 1) / (2 * kBQ);
+  const int n_kv = (n_tok + kBKV - 1) / kBKV;
+  if (n_kv > kPersistentMaxKeyTiles) {
+    using S = AttnSmem<HD, 1>;
+    auto kern = attn_tc_kernel<T, HD>;
+    static bool configured = false;
+    if (!configured) {
+      e = configure(kern, S::kBytes);
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    dim3 grid((unsigned)n_qp, (unsigned)BH);
+    kern<<<grid, kThreads, S::kBytes, s>>>(tq, tk, tv, (T*)out, n_head, n_tok, scale_log2, status);
+    return cudaGetLastError();
+  }
+  using S = AttnSmem<HD, 2>;
+  auto kern = attn_tc_persistent_kernel<T, HD>;
   static bool configured = false;
   if (!configured) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
+    e = configure(kern, S::kBytes);
     if (e != cudaSuccess) return e;
-    // setmaxnreg.inc waits until the registers it asks for are free within the
-    // block's launch allocation: refuse to launch when the allocation is short.
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs * kThreads < 128 * kRegsControl + 256 * kRegsSoftmax) return cudaErrorInvalidConfiguration;
     configured = true;
   }
   // persistent grid: one CTA per SM (its shared memory allows no second), each
   // taking every gridDim-th unit
-  const int n_units = (int)(((n_tok + 2 * kBQ - 1) / (2 * kBQ)) * BH);
+  const int n_units = (int)(n_qp * BH);
   const int slots = num_sms > 0 ? num_sms : 1;
   const int grid = n_units < slots ? n_units : slots;
-  kern<<<grid, kThreads, S::kBytes, s>>>(tq, tk, tv, (T*)out, n_head, n_tok, n_units, scale * 1.4426950408889634f,
-                                         status);
+  kern<<<grid, kThreads, S::kBytes, s>>>(tq, tk, tv, (T*)out, n_head, n_tok, n_units, scale_log2, status);
   return cudaGetLastError();
 }
 
