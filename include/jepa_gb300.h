@@ -22,8 +22,9 @@
  *     jepa_encoder_sync / jepa_predictor_sync reports it as
  *     JEPA_ERR_DEVICE_TIMEOUT.
  *   - Layouts are row-major, innermost dimension last.
- *   - Calls on one handle must not overlap in time (a handle owns one
- *     workspace).
+ *   - Calls on one handle must not overlap in time, on the host or on the
+ *     device (a handle owns one workspace): either every call on a handle
+ *     uses the same stream, or the caller synchronises before switching.
  */
 #ifndef JEPA_GB300_H
 #define JEPA_GB300_H
