@@ -28,15 +28,16 @@
 // idle; warps 4-7 softmax of Q0, warps 8-11 softmax of Q1 (warp w owns TMEM
 // lanes / query rows 32*(w%4) .. +31 of its tile).  One issuer per query tile
 // keeps each issuer's chain of waits and issues short: every SM
-// sub-partition also runs two softmax warps.  The first warpgroup hands registers to the softmax
-// warpgroups (setmaxnreg), which hold a whole 128-score row each.
+// sub-partition also runs two softmax warps.  The first warpgroup hands
+// registers to the softmax warpgroups (setmaxnreg), which hold a whole
+// 128-score row each.
 #include "internal.h"
 
 namespace jepa {
 
 namespace {
 
-constexpr int kBQ = 128;     // query rows per tile (two tiles per CTA)
+constexpr int kBQ = 128;     // query rows per tile (two tiles per unit)
 constexpr int kBKV = 128;    // keys per tile
 constexpr int kStages = 4;   // K/V ring depth
 constexpr int kThreads = 384;
@@ -50,7 +51,8 @@ static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "regist
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
 // Of every four exponent pairs, this many are evaluated by the FMA-pipe
-// polynomial and the rest by ex2.approx (balances the two pipes).
+// polynomial and the rest by ex2.approx.  0: every share measured slower,
+// the exponential loop being bound by instruction issue, not by ex2.
 constexpr int kPolyPairs = 0;
 
 template <int HD, int QBUF>
