@@ -36,8 +36,8 @@
 extern "C" {
 #endif
 
-#define JEPA_ABI_VERSION 4  /* 2: jepa_encoder_params.has_image_path; 3: 2.1 predictor fields;
-                               4: jepa_encode_host_async */
+#define JEPA_ABI_VERSION 5  /* 2: jepa_encoder_params.has_image_path; 3: 2.1 predictor fields;
+                               4: jepa_encode_host_async; 5: jepa_qkv_rope */
 
 #if defined(__GNUC__)
 #define JEPA_API __attribute__((visibility("default")))
@@ -302,9 +302,39 @@ JEPA_API jepa_status jepa_attention(const void* q, const void* k, const void* vt
 JEPA_API jepa_status jepa_linear(const void* A, const void* W, const float* bias, void* out, int M, int N, int K, int dtype,
                         int epilogue, void* stream);
 
+/* The fused QKV projection with 3-D RoPE, the first half of a block's
+ * attention ("V-JEPA 2 / 2.1 tensor maps and RoPE derivation", §2 fused
+ * attn_qkv with rows q;k;v and concat_heads; §4 RoPE on q and k after the
+ * bias: split d = 2*((head_dim//3)//2) per axis t, h, w, the last
+ * head_dim - 3d dims passed through; §4.1 tiled, §4.2 interleaved; §4.3
+ * positions p*(ref_grid-1)/(n-1) on the spatial axes; §4.4 positions taken
+ * from token ids).  The same kernels and epilogue as inside jepa_encode:
+ *   qkv[r, :] = A[r, :] W^T + bias,   r < M = batch*n_tokens;
+ *   q[b*n_head + h, i, :] = RoPE(qkv[b*n_tokens + i, h*hd : (h+1)*hd])
+ *   k[b*n_head + h, i, :] = RoPE(qkv[b*n_tokens + i, D + h*hd : ...])
+ *   vt[b*n_head + h, :, i] = qkv[b*n_tokens + i, 2D + h*hd : ...]
+ * with the position of row r the grid cell (t, h, w) of id pos_ids[r]
+ * (T-major in grid_t x grid_h x grid_w), or of id i = r mod n_tokens when
+ * pos_ids is NULL (then grid_t*grid_h*grid_w must equal n_tokens).  q and k
+ * are NOT scaled by 1/sqrt(head_dim): the attention applies the scale.
+ *   A: dtype [batch*n_tokens, D]; W: dtype [3D, D]; bias: float [3D] or NULL;
+ *   q, k: dtype [batch*n_head, n_tokens, head_dim]; vt: dtype
+ *   [batch*n_head, head_dim, ldv], ldv >= n_tokens, ldv % 8 == 0 (columns
+ *   >= n_tokens are not written); pos_ids: device int32 [batch*n_tokens] or
+ *   NULL; ids outside the grid are clamped and reported by jepa_ops_sync as
+ *   JEPA_ERR_ARG.
+ * D = embed_dim a multiple of 128 (<= 4096), head_dim = D/n_head 32 or 64;
+ * dtype F16/BF16 runs the tensor-core GEMM with the RoPE in its epilogue,
+ * F32 the CUDA-core GEMM.  All buffers are caller-owned device buffers. */
+JEPA_API jepa_status jepa_qkv_rope(const void* A, const void* W, const float* bias, void* q, void* k, void* vt,
+                                   int dtype, int batch, int n_tokens, int embed_dim, int n_head, int ldv,
+                                   int grid_t, int grid_h, int grid_w, int layout, int interpolate, int ref_grid,
+                                   float theta, const int32_t* pos_ids, void* stream);
+
 /* Synchronises `stream` and reports a device-side timeout recorded by any
- * earlier single-operation call (jepa_attention, jepa_linear) of this process
- * (then clears it). */
+ * earlier single-operation call (jepa_attention, jepa_linear, jepa_qkv_rope)
+ * of this process (then clears it), or ids outside the grid given to
+ * jepa_qkv_rope (JEPA_ERR_ARG). */
 JEPA_API jepa_status jepa_ops_sync(void* stream);
 
 /* Failure-detection self test: launches one kernel that waits on a barrier

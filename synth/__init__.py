@@ -188,7 +188,10 @@ def tensor_names_predictor(pc: PredictorConfig):
 
 
 def _one_tensor(args):
-    idx, (name, shape, kind), seed, storage, stream_base, std = args
+    idx, (name, shape, kind), seed, storage, stream_base, std, overrides = args
+    for suffix, s in overrides.items():
+        if name.endswith(suffix):
+            std = s
     n = int(np.prod(shape))
     if kind == "mat":
         v = round_to_dtype(normal(seed, stream_base + idx, n, std), storage)
@@ -201,19 +204,23 @@ def _one_tensor(args):
     return name, v.reshape(shape)
 
 
-def _materialise(names, seed, storage, stream_base, std=0.02):
+def _materialise(names, seed, storage, stream_base, std=0.02, overrides=None):
     # Tensors are independent streams, so they are drawn in parallel threads
     # (numpy releases the GIL); the values do not depend on the schedule.
     import concurrent.futures as cf
     import os
-    jobs = [(i, nk, seed, storage, stream_base, std) for i, nk in enumerate(names)]
+    jobs = [(i, nk, seed, storage, stream_base, std, dict(overrides or {})) for i, nk in enumerate(names)]
     with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
         return dict(ex.map(_one_tensor, jobs))
 
 
-def encoder_weights(cfg: EncoderConfig) -> dict:
-    """Random-init encoder weights (float32 arrays holding storage-dtype values)."""
-    return _materialise(tensor_names_encoder(cfg), cfg.seed, cfg.dtype, 1000)
+def encoder_weights(cfg: EncoderConfig, std_overrides: dict | None = None) -> dict:
+    """Random-init encoder weights (float32 arrays holding storage-dtype values).
+
+    ``std_overrides`` maps a tensor-name suffix (e.g. ``"attn_qkv.weight"``) to
+    the standard deviation its normal draws use instead of 0.02; the draws
+    come from the same streams, only scaled."""
+    return _materialise(tensor_names_encoder(cfg), cfg.seed, cfg.dtype, 1000, overrides=std_overrides)
 
 
 def predictor_weights(cfg: EncoderConfig) -> dict:

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
         assert n in SIGNATURES, f"binding lacks {n}"
-    assert lib.jepa_abi_version() == 4
+    assert lib.jepa_abi_version() == 5
 
 
 def _blob(cfg):
@@ -115,6 +115,16 @@ def test_argument_errors_without_gpu(lib):
     assert lib.jepa_linear(C.c_void_p(16), C.c_void_p(16), None, C.c_void_p(16), 8, 32, 40, 2, 0, None) == ERR_ARG
     assert lib.jepa_attention(C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), 2, 1, 1, 100, 64,
                               100, 0.125, None) == ERR_ARG          # ldv not a multiple of 8
+    v = C.c_void_p(16)
+    # jepa_qkv_rope: head_dim 48 unsupported; a grid that does not hold the
+    # tokens without ids; ldv not a multiple of 8; interpolation on a 1-wide grid
+    assert lib.jepa_qkv_rope(v, v, None, v, v, v, 2, 1, 64, 384, 8, 64, 1, 8, 8, 0, 0, 16, 1e4, None,
+                             None) == ERR_UNSUPPORTED
+    assert lib.jepa_qkv_rope(v, v, None, v, v, v, 2, 1, 65, 256, 4, 72, 1, 8, 8, 0, 0, 16, 1e4, None, None) == ERR_ARG
+    assert lib.jepa_qkv_rope(v, v, None, v, v, v, 2, 1, 64, 256, 4, 68, 1, 8, 8, 0, 0, 16, 1e4, None, None) == ERR_ARG
+    assert lib.jepa_qkv_rope(v, v, None, v, v, v, 2, 1, 64, 256, 4, 64, 4, 16, 1, 0, 1, 16, 1e4, None, None) == ERR_ARG
+    assert lib.jepa_qkv_rope(None, v, None, v, v, v, 2, 1, 64, 256, 4, 64, 1, 8, 8, 0, 0, 16, 1e4, None,
+                             None) == ERR_ARG
     assert lib.jepa_encoder_sync(None, None) == ERR_ARG
     assert lib.jepa_encode_host_async(None, C.c_void_p(16), 0, 1, 2, 16, 16, C.c_void_p(16), None, None) == ERR_ARG
     assert b"NULL" in lib.jepa_last_error()

@@ -357,3 +357,90 @@ def test_predictor_graph_replay(jg):
         pred.sync()
         assert torch.equal(out, refs[k][0]) and torch.equal(octx, refs[k][1]), k
     pred.close()
+
+
+@pytest.mark.parametrize("name", ["v2-hd32-sharp", "b21-hd64-sharp"])
+def test_sharp_attention_end_to_end(jg, name):
+    """Encoders whose attn_qkv.weight has std sqrt(3/D), so the attention
+    logits have std ~3 and the output depends on the RoPE: every clip, every
+    token, the taps and the token mean against the oracle.  The CPU test
+    tests/test_qkv_rope_controls.py shows that the oracle with the wrong
+    layout, without interpolation or without rotation fails these bars on the
+    same models."""
+    from qkv_cases import SHARP_MODELS, sharp_weights
+    cfg = SHARP_MODELS[name]
+    w = sharp_weights(cfg)
+    clip = synth.clip_u8(cfg)
+    enc = jg.Encoder(cfg, w)
+    res = enc.encode(torch.from_numpy(clip).cuda(), pooled=True, hier=True)
+    enc.sync()
+    got = {k: v.cpu().numpy() for k, v in res.items()}
+    for b in range(cfg.batch):
+        ref = oracle.encoder_forward(cfg, w, clip[b])
+        assert_close_16bit(got["out"][b], ref["out"], f"{name} clip {b}")
+        for k, tap in enumerate(ref["hier"]):
+            assert_close_16bit(got["hier"][k, b], tap, f"{name} tap {k} clip {b}")
+        np.testing.assert_allclose(got["pooled"][b], ref["pooled"], atol=1e-2 * np.abs(ref["pooled"]).max())
+    enc.close()
+
+
+@pytest.mark.parametrize("name", ["v2-hd32-sharp", "b21-hd64-sharp"])
+def test_sharp_attention_masked_encoder(jg, name):
+    """The masked encoder on the sharp-attention models: each clip keeps its
+    own random 45 % of the tokens in random order, so the RoPE positions come
+    from the ids; every kept token against the oracle's masked forward."""
+    from qkv_cases import SHARP_MODELS, sharp_weights
+    cfg = SHARP_MODELS[name]
+    w = sharp_weights(cfg)
+    clip = synth.clip_u8(cfg)
+    n = synth.tokens_per_clip(cfg)
+    K = int(n * 0.45)
+    keep = np.stack([np.random.default_rng(77 + b).choice(n, K, replace=False)
+                     for b in range(cfg.batch)]).astype(np.int32)
+    enc = jg.Encoder(cfg, w)
+    got = enc.encode_masked(torch.from_numpy(clip).cuda(), torch.from_numpy(keep).cuda())["out"].cpu().numpy()
+    enc.sync()
+    for b in range(cfg.batch):
+        ref = oracle.encoder_forward(cfg, w, clip[b], keep=keep[b])
+        assert_close_16bit(got[b], ref["out"], f"{name} masked clip {b}")
+    enc.close()
+
+
+def test_two_handles_two_threads(jg):
+    """Two encoder handles on device 0, used from two threads at the same
+    time, each on its own stream (the launch set-up kept per device is done
+    once under a lock; each handle has its own workspace and graphs).  Each
+    thread encodes three times (eager, captured, replayed); every result
+    matches the oracle and the three are identical."""
+    import threading
+    cfgs = [SMALL["b21-bf16"], SMALL["v2-hd32"]]
+    results, errors = [None, None], []
+
+    def work(i):
+        try:
+            cfg = cfgs[i]
+            w = synth.encoder_weights(cfg)
+            clip = synth.clip_u8(cfg)
+            s = torch.cuda.Stream()
+            enc = jg.Encoder(cfg, w)
+            with torch.cuda.stream(s):
+                c = torch.from_numpy(clip).cuda()
+                outs = [enc.encode(c, stream=s)["out"] for _ in range(3)]
+                enc.sync(s)
+                outs = [o.cpu().numpy() for o in outs]
+            enc.close()
+            results[i] = (cfg, w, clip, outs)
+        except Exception as e:  # reported below, in the test's thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for cfg, w, clip, outs in results:
+        np.testing.assert_array_equal(outs[1], outs[0])
+        np.testing.assert_array_equal(outs[2], outs[0])
+        for b in range(cfg.batch):
+            assert_close_16bit(outs[0][b], oracle.encoder_forward(cfg, w, clip[b])["out"], f"thread {cfg.name} {b}")

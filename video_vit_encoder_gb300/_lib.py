@@ -27,7 +27,7 @@ class JepaError(RuntimeError):
         self.status = status
 
 
-ABI_VERSION = 4  # JEPA_ABI_VERSION of include/jepa_gb300.h
+ABI_VERSION = 5  # JEPA_ABI_VERSION of include/jepa_gb300.h
 
 
 class EncoderParams(C.Structure):
@@ -74,6 +74,7 @@ SIGNATURES = {
     "jepa_rope3d_f32": (ST, [VP, I, I, I, I, I, I, I, I, I, I, F, VP]),
     "jepa_attention": (ST, [VP, VP, VP, VP, I, I, I, I, I, I, F, VP]),
     "jepa_linear": (ST, [VP, VP, VP, VP, I, I, I, I, I, VP]),
+    "jepa_qkv_rope": (ST, [VP, VP, VP, VP, VP, VP, I, I, I, I, I, I, I, I, I, I, I, I, F, VP, VP]),
     "jepa_ops_sync": (ST, [VP]),
     "jepa_selftest_wait_timeout": (ST, [I, VP]),
     "jepa_patch_embed_static": (ST, [VP, VP, VP, VP, VP, I, I, I, I, I, I, VP]),

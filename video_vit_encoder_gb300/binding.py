@@ -353,6 +353,31 @@ def linear(A, W, bias, epilogue: int, out=None):
     return out
 
 
+def qkv_rope(A, W, bias, batch: int, n_tokens: int, n_head: int, grid, layout: str, interpolate: bool = False,
+             ref_grid: int = 16, theta: float = 10000.0, pos_ids=None, out=None):
+    """Fused QKV projection + 3-D RoPE: A [batch*n_tokens, D], W [3D, D] in one
+    dtype, bias float [3D] or None, pos_ids int32 [batch*n_tokens] or None.
+    Returns (q, k, vt): q, k [batch*n_head, n_tokens, hd] and vt
+    [batch*n_head, hd, ldv] (columns >= n_tokens zeroed here, never written)."""
+    dt = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}[A.dtype]
+    D = A.shape[1]
+    hd = D // n_head
+    ldv = (n_tokens + 7) // 8 * 8
+    if out is None:
+        q = torch.empty((batch * n_head, n_tokens, hd), dtype=A.dtype, device=A.device)
+        k = torch.empty_like(q)
+        vt = torch.zeros((batch * n_head, hd, ldv), dtype=A.dtype, device=A.device)
+    else:
+        q, k, vt = out
+        ldv = vt.shape[-1]
+    gt, gh, gw = grid
+    ids = pos_ids.to(dtype=torch.int32).contiguous() if pos_ids is not None else None
+    check(load().jepa_qkv_rope(_ptr(A), _ptr(W), _ptr(bias), _ptr(q), _ptr(k), _ptr(vt), DTYPE_CODE[dt], batch,
+                               n_tokens, D, n_head, ldv, gt, gh, gw, LAYOUT_CODE[layout], int(bool(interpolate)),
+                               ref_grid, theta, _ptr(ids), _stream()))
+    return q, k, vt
+
+
 def ops_sync():
     check(load().jepa_ops_sync(_stream()))
 

@@ -521,14 +521,35 @@ __global__ void add_vec_kernel(float* a, const float* b, int n) {
   if (i < n) a[i] += b[i];
 }
 
-int* g_ops_status = nullptr;  // device status word of the single operations
+// Device status word of the single operations, one per device (allocated on
+// the first single-operation call made with that device current).
+DeviceOnce g_ops_once;
+int* g_ops_status[kMaxDevices] = {};
 jepa_status ops_status(int** out) {
-  if (g_ops_status == nullptr) {
-    if (cudaMalloc(&g_ops_status, sizeof(int)) != cudaSuccess) return fail(JEPA_ERR_OOM, "status word");
-    if (cudaMemset(g_ops_status, 0, sizeof(int)) != cudaSuccess) return fail(JEPA_ERR_CUDA, "status word");
-  }
-  *out = g_ops_status;
+  int dev = 0;
+  const cudaError_t e = g_ops_once.run([](int d) -> cudaError_t {
+    int* p = nullptr;
+    cudaError_t r = cudaMalloc(&p, sizeof(int));
+    if (r != cudaSuccess) return r;
+    r = cudaMemset(p, 0, sizeof(int));
+    if (r != cudaSuccess) {
+      cudaFree(p);
+      return r;
+    }
+    g_ops_status[d] = p;
+    return cudaSuccess;
+  }, &dev);
+  if (e != cudaSuccess) return fail(JEPA_ERR_CUDA, "single-operation status word: %s", cudaGetErrorString(e));
+  *out = g_ops_status[dev];
   return JEPA_OK;
+}
+
+// RoPE tables of the single operations, per calling thread and device.
+RopeCache& ops_rope_cache() {
+  static thread_local RopeCache rc[kMaxDevices];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return rc[dev >= 0 && dev < kMaxDevices ? dev : 0];
 }
 
 jepa_status read_status(int* d_status, cudaStream_t s) {
@@ -1391,7 +1412,7 @@ jepa_status jepa_rope3d_f32(float* x, int batch, int n_tokens, int n_head, int h
   if (interpolate && (grid_h < 2 || grid_w < 2 || ref_grid < 2))
     return fail(JEPA_ERR_ARG, "interpolation needs a grid and reference wider than 1");
   if (!(theta > 0.f)) return fail(JEPA_ERR_ARG, "theta must be > 0");
-  static thread_local RopeCache rc;
+  RopeCache& rc = ops_rope_cache();
   cudaStream_t s = (cudaStream_t)stream;
   JEPA_TRY(rope_prepare(rc, head_dim, layout, theta, grid_t, grid_h, grid_w, interpolate, ref_grid, s));
   if (batch == 0) return JEPA_OK;
@@ -1441,6 +1462,54 @@ jepa_status jepa_linear(const void* A, const void* W, const float* bias, void* o
   ep.out = out;
   ep.ldo = N;
   return run_linear(dtype, epilogue, A, W, M, N, K, ep, st, (cudaStream_t)stream, sms);
+}
+
+jepa_status jepa_qkv_rope(const void* A, const void* W, const float* bias, void* q, void* k, void* vt, int dtype,
+                          int batch, int n_tokens, int embed_dim, int n_head, int ldv, int grid_t, int grid_h,
+                          int grid_w, int layout, int interpolate, int ref_grid, float theta, const int32_t* pos_ids,
+                          void* stream) {
+  if (!A || !W || !q || !k || !vt) return fail(JEPA_ERR_ARG, "NULL buffer");
+  if (!aligned16(A) || !aligned16(W) || !aligned16(bias) || !aligned16(q) || !aligned16(k) || !aligned16(vt))
+    return fail(JEPA_ERR_ARG, "buffers must be 16-byte aligned");
+  if (dtype < 0 || dtype > 2) return fail(JEPA_ERR_ARG, "dtype %d", dtype);
+  JEPA_TRY(check_width(embed_dim, n_head, 64, dtype, "qkv_rope"));
+  const int hd = embed_dim / n_head;
+  if (batch < 1 || n_tokens < 1) return fail(JEPA_ERR_ARG, "batch %d and n_tokens %d must be >= 1", batch, n_tokens);
+  if (grid_t < 1 || grid_h < 1 || grid_w < 1) return fail(JEPA_ERR_ARG, "grid %dx%dx%d", grid_t, grid_h, grid_w);
+  const long long cells = (long long)grid_t * grid_h * grid_w;
+  if (pos_ids == nullptr && cells != n_tokens)
+    return fail(JEPA_ERR_ARG, "grid %dx%dx%d does not hold %d tokens (give pos_ids for a subset)", grid_t, grid_h,
+                grid_w, n_tokens);
+  if (cells >= (1ll << 31)) return fail(JEPA_ERR_ARG, "grid too large");
+  if (ldv < n_tokens || ldv % 8 != 0) return fail(JEPA_ERR_ARG, "ldv %d must be >= n_tokens and a multiple of 8", ldv);
+  if ((long long)batch * n_tokens * 3 * embed_dim >= (1ll << 31)) return fail(JEPA_ERR_ARG, "too many rows");
+  if (layout != 0 && layout != 1) return fail(JEPA_ERR_ARG, "layout %d", layout);
+  if (interpolate && (grid_h < 2 || grid_w < 2 || ref_grid < 2))
+    return fail(JEPA_ERR_ARG, "interpolation needs a grid and reference wider than 1");
+  if (!(theta > 0.f)) return fail(JEPA_ERR_ARG, "theta must be > 0");
+  int* st = nullptr;
+  JEPA_TRY(ops_status(&st));
+  cudaStream_t s = (cudaStream_t)stream;
+  RopeCache& rc = ops_rope_cache();
+  JEPA_TRY(rope_prepare(rc, hd, layout, theta, grid_t, grid_h, grid_w, interpolate, ref_grid, s));
+  const int M = batch * n_tokens;
+  if (pos_ids != nullptr) JEPA_TRY(cuda_status(check_ids(pos_ids, M, (int)cells, st, s), "id check"));
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  EpiParams ep{};
+  ep.bias = bias;
+  ep.q = q;
+  ep.k = k;
+  ep.vt = vt;
+  ep.n_tok = n_tokens;
+  ep.n_head = n_head;
+  ep.head_dim = hd;
+  ep.ldv = ldv;
+  ep.dmodel = embed_dim;
+  ep.pos_ids = pos_ids;
+  ep.rope = rc.rp;
+  return run_linear(dtype, EPI_QKV, A, W, M, 3 * embed_dim, embed_dim, ep, st, s, sms);
 }
 
 jepa_status jepa_ops_sync(void* stream) {

@@ -2,7 +2,7 @@
 
     python -m video_vit_encoder_gb300.opbench OP [--reps R] [--warmup W]
 
-OP is one of attention, qkv, out_proj, ffn_up, ffn_down, layernorm, and
+OP is one of attention, qkv (the QKV GEMM with its RoPE epilogue), out_proj, ffn_up, ffn_down, layernorm, and
 out_proj_f32 / out_proj_bf16 (the out_proj shape with a plain fp32 or 16-bit
 store instead of the residual add), and predictor21: the whole V-JEPA 2.1
 masked predictor (D 384, 12 blocks, head_dim 32, FFN 1536, out 1664, context
@@ -56,12 +56,23 @@ def _setup(op):
         fl = (2 * len(ctx) * pc.in_dim * pd + pl * (2 * n * (4 * pd * pd + 2 * pd * pf) + 4 * n * n * pd)
               + 2 * n * pd * pc.out_dim)
         return (lambda: pred.predict(enc, ic, it, grid, modality="video", with_ctx=True)), fl, "TFLOP/s"
+    if op == "qkv":
+        # the fused QKV GEMM with its 3-D RoPE epilogue (tiled, 8 x 16 x 16 grid), head-major q/k and v^T
+        A = rnd(M, D)
+        W = rnd(3 * D, D, scale=0.02)
+        bias = torch.zeros(3 * D, device="cuda")
+        hd = D // H
+        q = torch.empty(B * H, N, hd, dtype=bf, device="cuda")
+        k = torch.empty_like(q)
+        vt = torch.zeros(B * H, hd, N, dtype=bf, device="cuda")
+        return (lambda: jb.qkv_rope(A, W, bias, B, N, H, (8, 16, 16), "tiled", out=(q, k, vt))), \
+            2.0 * M * 3 * D * D, "TFLOP/s"
     if op == "layernorm":
         x = rnd(M, D, dtype=torch.float32)
         w, b = torch.ones(D, device="cuda"), torch.zeros(D, device="cuda")
         y = torch.empty_like(x)
         return (lambda: jb.layernorm_f32(x, w, b, 1e-6, out=y)), 8.0 * M * D, "GB/s"
-    shapes = {"qkv": (3 * D, D, 0), "out_proj": (D, D, 2), "ffn_up": (F, D, 3), "ffn_down": (D, F, 2),
+    shapes = {"out_proj": (D, D, 2), "ffn_up": (F, D, 3), "ffn_down": (D, F, 2),
               "out_proj_f32": (D, D, 1), "out_proj_bf16": (D, D, 0)}
     n, kdim, epi = shapes[op]
     A = rnd(M, kdim)
