@@ -808,24 +808,18 @@ cudaError_t launch_t(const void* q, const void* k, const void* vt, void* out, in
   if (n_kv > kPersistentMaxKeyTiles) {
     using S = AttnSmem<HD, 1>;
     auto kern = attn_tc_kernel<T, HD>;
-    static bool configured = false;
-    if (!configured) {
-      e = configure(kern, S::kBytes);
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
+    static DeviceOnce setup;   // the shared-memory opt-in is per device
+    e = setup.run([&](int) { return configure(kern, S::kBytes); });
+    if (e != cudaSuccess) return e;
     dim3 grid((unsigned)n_qp, (unsigned)BH);
     kern<<<grid, kThreads, S::kBytes, s>>>(tq, tk, tv, (T*)out, n_head, n_tok, scale_log2, status);
     return cudaGetLastError();
   }
   using S = AttnSmem<HD, 2>;
   auto kern = attn_tc_persistent_kernel<T, HD>;
-  static bool configured = false;
-  if (!configured) {
-    e = configure(kern, S::kBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static DeviceOnce setup;
+  e = setup.run([&](int) { return configure(kern, S::kBytes); });
+  if (e != cudaSuccess) return e;
   // persistent grid: one CTA per SM (its shared memory allows no second), each
   // taking every gridDim-th unit
   const int n_units = (int)(n_qp * BH);

@@ -603,31 +603,39 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
                        const EpiParams& ep, int* status, cudaStream_t stream, int num_sms) {
   using S = GemmSmem<BN, STAGES, CM>;
   auto kern = gemm_tc_kernel<T, BN, STAGES, EPI, QHD, QLAYOUT, CM>;
-  static bool configured = false;  // per instantiation
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = S::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Per device and instantiation: the shared-memory opt-in and, for CTA
+  // pairs, how many pairs can be resident at once (the persistent grid's size).
+  static DeviceOnce setup;
+  static int resident_on[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = setup.run([&](int d) -> cudaError_t {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
+    if (r != cudaSuccess) return r;
+    int resident = num_sms / 2;
+    if constexpr (CM == 2) {
+      cudaLaunchConfig_t probe = cfg;
+      probe.gridDim = dim3(2 * (num_sms / 2));
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &probe) == cudaSuccess && n >= 1) resident = n;
+    }
+    resident_on[d] = resident;
+    return cudaSuccess;
+  }, &dev);
+  if (e != cudaSuccess) return e;
   const int num_m = (M + kBM - 1) / kBM, num_n = (N + BN - 1) / BN;
   if constexpr (CM == 2) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = S::kBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // The persistent grid holds only as many pairs as can be resident at once.
-    static int resident = 0;  // per instantiation
-    if (resident == 0) {
-      cfg.gridDim = dim3(2 * (num_sms / 2));
-      if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) resident = num_sms / 2;
-    }
+    const int resident = resident_on[dev];
     const int tiles = ((num_m + 1) / 2) * num_n;
     const int tail_start = split_tail_start<BN, EPI, QHD>(tiles, resident);
     const int units = tail_start + 2 * (tiles - tail_start);

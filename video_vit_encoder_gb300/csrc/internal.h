@@ -5,9 +5,42 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace jepa {
+
+// Launch set-up that the runtime keeps per device (the opt-in to more than
+// 48 KB of dynamic shared memory, occupancy figures, SM counts) is done once
+// per device and per call site, under a lock, so handles on different devices
+// of one process, and threads launching at the same time, each see it done
+// for their own device.  `init(dev)` runs with `dev` current; a failed init
+// is retried by the next call.  State it computes goes into arrays indexed by
+// the device, written before `done` is released and read after it.
+constexpr int kMaxDevices = 64;
+class DeviceOnce {
+ public:
+  template <typename F>
+  cudaError_t run(F&& init, int* dev_out = nullptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (dev_out != nullptr) *dev_out = dev;
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = init(dev);
+    if (e == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  std::mutex mu_;
+  std::atomic<bool> done_[kMaxDevices] = {};
+};
 
 // dtype codes of the ABI (jepa_dtype)
 enum : int { DTYPE_F32 = 0, DTYPE_F16 = 1, DTYPE_BF16 = 2 };

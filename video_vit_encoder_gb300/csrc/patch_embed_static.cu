@@ -39,7 +39,7 @@ constexpr size_t kStaticScratchBytes = (size_t)kStaticMaxRows * 1536 * 2;
 static __device__ __align__(256) uint8_t g_patch_scratch[kStaticScratchBytes];
 static __device__ int g_patch_status;
 
-constexpr int kMaxDevices = 64;
+using jepa::kMaxDevices;
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 int* g_status_addr[kMaxDevices] = {};

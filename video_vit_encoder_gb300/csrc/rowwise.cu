@@ -168,12 +168,17 @@ cudaError_t layernorm_t(const float* x, const float* w, const float* b, void* y,
                         cudaStream_t s) {
   const int nv = dim / 128;
   // persistent: 2 blocks of 8 warps per SM, each warp striding over ~rows/2432 rows
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 132;
-  }
+  static DeviceOnce setup;
+  static int sms_on[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = setup.run([](int d) {
+    int n = 0;
+    const cudaError_t r = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    sms_on[d] = (r == cudaSuccess && n >= 1) ? n : 1;
+    return r;
+  }, &dev);
+  if (e != cudaSuccess) return e;
+  const int sms = sms_on[dev];
   const int need = (rows + 7) / 8;
   const int blocks = need < 2 * sms ? need : 2 * sms;
   T* yy = reinterpret_cast<T*>(y);
