@@ -50,3 +50,20 @@ def test_traffic_used_only_for_the_profiled_source():
         assert got is None
     assert b._traffic_for("attention", "another launch") is None
     assert b._traffic_for("no such kernel", rec["launch"]) is None
+
+
+def test_reference_arm_steps_are_measured_half_clips():
+    """The oracle arm's steps are halves of one clip's forward, alternating on
+    the carried residual: the line's time is what the steps measured
+    (ms_per_step x steps is the timed work) and two steps make one clip."""
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "vitb16-img384",
+                        "--steps", "2", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3
+    n_tok = synth.tokens_per_clip(synth.CONFIGS["img384"])
+    # value = one whole clip's tokens over the two steps' measured time
+    assert abs(line["value"] * line["ms_per_step"] * 2 / 1000.0 - n_tok) < 1e-6 * n_tok
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["host_cores"] >= 1
+    assert "every two steps encode one whole clip" in cb["sample"]
