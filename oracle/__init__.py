@@ -14,5 +14,5 @@ from .encoder import (  # noqa: F401
     rot90_pairs, apply_rope, layer_norm, gelu_erf, attention_heads,
     block_forward, block_forward_rows, encoder_forward, predictor_forward,
     grid_positions_from_ids, predictor_input, encoder_rope, encoder_embed, is_image,
-    predictor_outputs,
+    predictor_outputs, attentive_pool_forward,
 )

@@ -1,4 +1,5 @@
-"""Plain float64 restatement of the V-JEPA 2 / 2.1 encoder and masked predictor.
+"""Plain float64 restatement of the V-JEPA 2 / 2.1 encoder, masked predictor
+and attentive-pool classifier head.
 
 TEST INFRASTRUCTURE ONLY (see the package docstring).  Parity of every
 function here is pinned by ``tests/test_oracle_*.py`` against library
@@ -8,8 +9,8 @@ composition" because no worked example with synthetic weights exists.
 
 Sources (page title, section):
   [N]  "V-JEPA 2 / 2.1 tensor maps and RoPE derivation" (jepa.cpp conversion
-       notes): §1 hyper-parameters, §2 HF key map, §3 2.1 encoder/predictor
-       forward, §4 3-D RoPE (4.1 tiled, 4.2 interleaved, 4.3 interpolation,
+       notes): §1 hyper-parameters, §2 HF key map and "Attentive-pool head -
+       exact forward", §3 2.1 encoder/predictor forward, §4 3-D RoPE (4.1 tiled, 4.2 interleaved, 4.3 interpolation,
        4.4 predictor ids), §5 preprocessing.
   [P]  "Parity - image ViT encoders ... and video encoders" (jepa.cpp parity
        report): "Preprocessing parity" (fused normalisation form),
@@ -367,3 +368,38 @@ def predictor_outputs(pcfg, pwts, enc_out, ids_ctx, ids_tgt, grid, modality: str
 def predictor_forward(pcfg, pwts, enc_out, ids_ctx, ids_tgt, grid, modality: str = "video"):
     """The target predictions of :func:`predictor_outputs`."""
     return predictor_outputs(pcfg, pwts, enc_out, ids_ctx, ids_tgt, grid, modality)["pred"]
+
+
+# ----------------------------------------------------------------------------- attentive-pool head
+def attentive_pool_forward(hcfg, hwts, enc_out):
+    """Attentive-pool head and classifier of ONE clip ([N] §2, "Attentive-pool
+    head - exact forward"; [N] §1 head row: 3 pool layers, 174 classes).
+
+    x = enc_out (after enc.norm); n_layer pre-LN self-attention blocks with NO
+    RoPE; then one cross-attention whose single query is the raw learned token
+    head.query (not normalised), keys and values from ln_kv(x), separate q/k/v
+    projections, softmax(q_h k_h^T / sqrt(head_dim)) v_h concatenated over the
+    heads with no output projection; the residual is the raw query; then
+    y += ffn_down(gelu(ffn_up(ln2(y)))); logits = y W_cls^T + b_cls with no
+    final norm.  Returns ``pooled`` = y (the classifier input) and ``logits``.
+    """
+    x = np.asarray(enc_out, F64)
+    N, D = x.shape
+    hd = D // hcfg.n_head
+    # no RoPE in the pool blocks: the identity rotation (COS 1, SIN 0)
+    ones, zeros = np.ones((N, hd), F64), np.zeros((N, hd), F64)
+    for i in range(hcfg.n_layer):
+        x = block_forward(x, hwts, i, hcfg.n_head, hcfg.ln_eps, ones, zeros, prefix="head.blk.")
+    q0 = np.asarray(hwts["head.query"], F64).reshape(1, D)
+    kv = layer_norm(x, hwts["head.xattn.ln_kv.weight"], hwts["head.xattn.ln_kv.bias"], hcfg.ln_eps)
+    q = _linear(q0, hwts["head.xattn.q.weight"], hwts["head.xattn.q.bias"])
+    k = _linear(kv, hwts["head.xattn.k.weight"], hwts["head.xattn.k.bias"])
+    v = _linear(kv, hwts["head.xattn.v.weight"], hwts["head.xattn.v.bias"])
+    o = attention_heads(_split_heads(q, hcfg.n_head), _split_heads(k, hcfg.n_head), _split_heads(v, hcfg.n_head))
+    o = o.transpose(1, 0, 2).reshape(1, D)             # heads concatenated; no output projection
+    y = q0 + o                                         # the residual is the raw query
+    yn = layer_norm(y, hwts["head.xattn.ln2.weight"], hwts["head.xattn.ln2.bias"], hcfg.ln_eps)
+    y = y + _linear(gelu_erf(_linear(yn, hwts["head.xattn.ffn_up.weight"], hwts["head.xattn.ffn_up.bias"])),
+                    hwts["head.xattn.ffn_down.weight"], hwts["head.xattn.ffn_down.bias"])
+    logits = _linear(y, hwts["head.cls.weight"], hwts["head.cls.bias"])
+    return {"pooled": y[0], "logits": logits[0]}

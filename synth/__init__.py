@@ -21,10 +21,11 @@ from __future__ import annotations
 
 import numpy as np
 
-from .configs import CONFIGS, PREDICTOR_21, EncoderConfig, PredictorConfig, tokens_per_clip
+from .configs import CONFIGS, HEAD_SSV2, PREDICTOR_21, EncoderConfig, HeadConfig, PredictorConfig, tokens_per_clip
 
 __all__ = [
-    "GOLDEN", "CONFIGS", "PREDICTOR_21", "EncoderConfig", "PredictorConfig", "tokens_per_clip",
+    "GOLDEN", "CONFIGS", "PREDICTOR_21", "HEAD_SSV2", "EncoderConfig", "HeadConfig", "PredictorConfig",
+    "tokens_per_clip", "tensor_names_head", "head_weights",
     "mix64", "draws_u64", "uniform_u8", "normal", "round_to_dtype",
     "bf16_bits", "f16_bits", "bits_to_f32",
     "encoder_weights", "predictor_weights", "clip_u8", "context_target_split",
@@ -187,6 +188,35 @@ def tensor_names_predictor(pc: PredictorConfig):
     return out
 
 
+def tensor_names_head(hc: HeadConfig):
+    """The attentive-pool head's tensors in blob order (conversion notes §2
+    head rows): the learned query, the pool blocks (encoder block layout, q/k/v
+    fused), the cross-attention block (ln_kv, separate q/k/v projections, ln2,
+    MLP) and the classifier."""
+    D, F, C = hc.embed_dim, hc.ffn_dim, hc.n_classes
+    out = [("head.query", (D,), "vec")]
+    for i in range(hc.n_layer):
+        p = f"head.blk.{i}."
+        out += [
+            (p + "ln1.weight", (D,), "one"), (p + "ln1.bias", (D,), "zero"),
+            (p + "attn_qkv.weight", (3 * D, D), "mat"), (p + "attn_qkv.bias", (3 * D,), "zero"),
+            (p + "attn_out.weight", (D, D), "mat"), (p + "attn_out.bias", (D,), "zero"),
+            (p + "ln2.weight", (D,), "one"), (p + "ln2.bias", (D,), "zero"),
+            (p + "ffn_up.weight", (F, D), "mat"), (p + "ffn_up.bias", (F,), "zero"),
+            (p + "ffn_down.weight", (D, F), "mat"), (p + "ffn_down.bias", (D,), "zero"),
+        ]
+    x = "head.xattn."
+    out += [(x + "ln_kv.weight", (D,), "one"), (x + "ln_kv.bias", (D,), "zero"),
+            (x + "q.weight", (D, D), "mat"), (x + "q.bias", (D,), "zero"),
+            (x + "k.weight", (D, D), "mat"), (x + "k.bias", (D,), "zero"),
+            (x + "v.weight", (D, D), "mat"), (x + "v.bias", (D,), "zero"),
+            (x + "ln2.weight", (D,), "one"), (x + "ln2.bias", (D,), "zero"),
+            (x + "ffn_up.weight", (F, D), "mat"), (x + "ffn_up.bias", (F,), "zero"),
+            (x + "ffn_down.weight", (D, F), "mat"), (x + "ffn_down.bias", (D,), "zero"),
+            ("head.cls.weight", (C, D), "mat"), ("head.cls.bias", (C,), "zero")]
+    return out
+
+
 def _one_tensor(args):
     idx, (name, shape, kind), seed, storage, stream_base, std, overrides = args
     for suffix, s in overrides.items():
@@ -226,6 +256,21 @@ def encoder_weights(cfg: EncoderConfig, std_overrides: dict | None = None) -> di
 def predictor_weights(cfg: EncoderConfig) -> dict:
     pc = cfg.predictor
     return _materialise(tensor_names_predictor(pc), cfg.seed, cfg.dtype, 500000)
+
+
+def head_weights(hc: HeadConfig, seed: int, dtype: str, std_overrides: dict | None = None,
+                 kind_overrides: dict | None = None) -> dict:
+    """Random-init attentive-pool head weights: matrices and the query
+    N(0, 0.02) (matrices rounded to ``dtype``), biases 0, LayerNorm 1 / 0;
+    streams of their own (base 700000), so no encoder or predictor tensor
+    moves.  ``std_overrides`` maps a name suffix to another standard
+    deviation; ``kind_overrides`` a name suffix to another kind ("mat",
+    "vec", "zero", "one"), e.g. non-zero biases."""
+    names = tensor_names_head(hc)
+    if kind_overrides:
+        names = [(n, sh, next((k for suf, k in kind_overrides.items() if n.endswith(suf)), kind))
+                 for n, sh, kind in names]
+    return _materialise(names, seed, dtype, 700000, overrides=std_overrides)
 
 
 def clip_u8(cfg: EncoderConfig, batch: int | None = None, first_clip: int = 0) -> np.ndarray:

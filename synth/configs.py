@@ -38,6 +38,25 @@ PREDICTOR_21 = PredictorConfig(in_dim=768, out_dim=1664, n_mask_tokens=8, rope_l
 
 
 @dataclass(frozen=True)
+class HeadConfig:
+    """Attentive-pool head + classifier (conversion notes §1 head row and §2
+    "Attentive-pool head - exact forward"): the SSv2 ViT-L/16 classifier's
+    head, 3 pre-LN self-attention pool blocks (16 heads, head_dim 64, no
+    RoPE), one single-query cross-attention block, 174 classes.  The pool
+    blocks' FFN width is 4 x D, the encoder's MLP ratio (the pages do not print
+    it)."""
+    embed_dim: int = 1024
+    n_layer: int = 3
+    n_head: int = 16
+    ffn_dim: int = 4096
+    n_classes: int = 174
+    ln_eps: float = 1e-6
+
+
+HEAD_SSV2 = HeadConfig()
+
+
+@dataclass(frozen=True)
 class EncoderConfig:
     name: str
     workload: str

@@ -5,7 +5,9 @@ At these sizes the oracle checks what it can compute in seconds:
     to end on every token, clip 7 block by block on sampled rows;
   * img384 (2.1 native image path, 32 images of 384 px) - two images end to
     end on every token, with the hierarchical taps;
-  * c2, c4, c5 - block by block on sampled rows (each block recomputed by the
+  * c2 (2.1 ViT-B/16, fp16, one 16 x 384 x 384 clip) - end to end on every
+    token, and block by block on sampled rows;
+  * c4, c5 - block by block on sampled rows (each block recomputed by the
     oracle from the GPU's own input residual), the final norm and the
     hierarchical taps on sampled rows, and the c4 predictor end to end.
 """
@@ -107,6 +109,24 @@ def test_c2_blocks_and_final(jg):
     xr = x.cpu().numpy().astype(np.float64)[rows]
     ref = oracle.layer_norm(xr, w["norm.weight"], w["norm.bias"], cfg.ln_eps)
     assert_close_16bit(out[0].cpu().numpy()[rows], ref, "c2 final norm")
+    enc.close()
+
+
+def test_c2_end_to_end(jg):
+    """The 2.1 ViT-B/16 fp16 workload (12 layers, interleaved RoPE
+    interpolated to the 16-grid, modality vector, one 16 x 384 x 384 clip of
+    4608 tokens) end to end on every token against the oracle, so error that
+    grows through the 12 layers is compared too."""
+    cfg = synth.CONFIGS["c2"]
+    w = _weights("c2")
+    clip = synth.clip_u8(cfg)
+    enc = jg.Encoder(cfg, w)
+    res = enc.encode(torch.from_numpy(clip).cuda(), pooled=True)
+    enc.sync()
+    ref = oracle.encoder_forward(cfg, w, clip[0])
+    m = assert_close_16bit(res["out"][0].cpu().numpy(), ref["out"], "c2 end to end")
+    print("c2 end to end:", m)
+    np.testing.assert_allclose(res["pooled"][0].cpu().numpy(), ref["pooled"], atol=1e-2 * np.abs(ref["pooled"]).max())
     enc.close()
 
 
