@@ -36,8 +36,8 @@
 extern "C" {
 #endif
 
-#define JEPA_ABI_VERSION 5  /* 2: jepa_encoder_params.has_image_path; 3: 2.1 predictor fields;
-                               4: jepa_encode_host_async; 5: jepa_qkv_rope */
+#define JEPA_ABI_VERSION 6  /* 2: jepa_encoder_params.has_image_path; 3: 2.1 predictor fields;
+                               4: jepa_encode_host_async; 5: jepa_qkv_rope; 6: attentive-pool head */
 
 #if defined(__GNUC__)
 #define JEPA_API __attribute__((visibility("default")))
@@ -261,6 +261,51 @@ JEPA_API jepa_status jepa_predictor_sync(jepa_predictor* pred, void* stream);
  * as jepa_encoder_set_graphs (on by default; the id buffers are read at run
  * time, so a replay sees their current contents). */
 JEPA_API jepa_status jepa_predictor_set_graphs(jepa_predictor* pred, int on);
+
+/* ---------------------------------------------------------------- attentive-pool head
+ * The attentive-pool head and classifier on top of the encoder ("V-JEPA 2 /
+ * 2.1 tensor maps and RoPE derivation", §1 head row: 3 pool layers, 174
+ * classes for the SSv2 ViT-L/16 classifier; §2 key map head rows and
+ * "Attentive-pool head - exact forward"), per clip:
+ *   x = the clip's encoder tokens [N, D] (after enc.norm);
+ *   n_layer pre-LN self-attention blocks on x, laid out like the encoder's
+ *   blocks (fused q;k;v), with NO RoPE;
+ *   q = query Wq^T + bq (the raw learned token, not normalised);
+ *   kv = ln_kv(x); k = kv Wk^T + bk; v = kv Wv^T + bv;
+ *   o = concat_h softmax(q_h k_h^T / sqrt(64)) v_h (no output projection);
+ *   y = query + o; y += ffn_down(gelu(ffn_up(ln2(y))));
+ *   pooled = y; logits = y Wcls^T + bcls (no final norm).
+ * head_dim (embed_dim / n_head) must be 64 and embed_dim 256, 512, 768 or
+ * 1024.  dtype as for the encoder: the storage type of the 2-D matrices and
+ * of the pool blocks' matrix-multiply inputs; the cross-attention and the
+ * per-clip tail run in fp32.
+ * Blob tensor order (the §2 head names): query [D] (fp32); per pool block
+ * the encoder block's 12 tensors (ln1, attn_qkv, attn_out, ln2, ffn_up,
+ * ffn_down); xattn.ln_kv.weight/bias [D]; xattn.q.weight [D,D], .bias [D];
+ * xattn.k.*, xattn.v.* likewise; xattn.ln2.weight/bias [D];
+ * xattn.ffn_up.weight [F,D], .bias [F]; xattn.ffn_down.weight [D,F],
+ * .bias [D]; cls.weight [n_classes,D], cls.bias [n_classes]. */
+typedef struct jepa_head_params {
+  int embed_dim, n_layer, n_head, ffn_dim, n_classes;
+  float ln_eps;
+  int dtype;
+} jepa_head_params;
+typedef struct jepa_head jepa_head;
+JEPA_API jepa_status jepa_head_blob_check(const void* blob, size_t blob_bytes, const jepa_head_params* params);
+/* Validates params and the host blob, makes `device` current, copies the
+ * weights to device memory (owned by the handle until jepa_head_destroy) and
+ * derives the query's projections from them.  The blob may be freed after. */
+JEPA_API jepa_status jepa_head_create(const void* blob, size_t blob_bytes, const jepa_head_params* params,
+                                      int device, jepa_head** out);
+JEPA_API void jepa_head_destroy(jepa_head* head);
+/* tokens: device float [batch, n_tokens, D] (jepa_encode's out_tokens; not
+ * modified); logits: device float [batch, n_classes]; pooled: device float
+ * [batch, D] (the classifier input) or NULL.  Clips are independent.  The
+ * handle grows its device workspace on the first call with a larger shape. */
+JEPA_API jepa_status jepa_head_forward(jepa_head* head, const float* tokens, int batch, int n_tokens, float* logits,
+                                       float* pooled, void* stream);
+/* Synchronises `stream` and reports a device-side timeout of an earlier call. */
+JEPA_API jepa_status jepa_head_sync(jepa_head* head, void* stream);
 
 /* ---------------------------------------------------------------- single operations
  * The kernels of the encoder, callable one at a time (the same code runs

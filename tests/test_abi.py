@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
         assert n in SIGNATURES, f"binding lacks {n}"
-    assert lib.jepa_abi_version() == 5
+    assert lib.jepa_abi_version() == 6
 
 
 def _blob(cfg):
@@ -149,3 +149,23 @@ def test_predictor21_blob(lib):
         q = jg.predictor_params(pc, cfg.dtype)
         setattr(q, field, 0)
         assert lib.jepa_predictor_blob_check(blob, len(blob), C.byref(q)) == ERR_BLOB
+
+
+def test_head_blob(lib):
+    """The attentive-pool head's blob: the learned query, the pool blocks, the
+    cross-attention block and the classifier, in the header's order; params
+    must match it, and only head_dim 64 is supported."""
+    import video_vit_encoder_gb300 as jg
+    from video_vit_encoder_gb300._lib import ERR_BLOB, ERR_UNSUPPORTED, check
+    hc = synth.HeadConfig(embed_dim=256, n_layer=2, n_head=4, ffn_dim=512, n_classes=11)
+    w = synth.head_weights(hc, 0, "bf16")
+    order = jg.head_tensor_order(hc)
+    assert [n for n, _ in order] == [n for n, _, _ in synth.tensor_names_head(hc)]
+    blob = jg.pack_blob(order, w, "bf16")
+    p = jg.head_params(hc, "bf16")
+    check(lib.jepa_head_blob_check(blob, len(blob), C.byref(p)))
+    p.n_classes = 12
+    assert lib.jepa_head_blob_check(blob, len(blob), C.byref(p)) == ERR_BLOB
+    p = jg.head_params(hc, "bf16")
+    p.n_head = 8   # head_dim 32
+    assert lib.jepa_head_blob_check(blob, len(blob), C.byref(p)) == ERR_UNSUPPORTED

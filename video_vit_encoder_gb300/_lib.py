@@ -27,7 +27,7 @@ class JepaError(RuntimeError):
         self.status = status
 
 
-ABI_VERSION = 5  # JEPA_ABI_VERSION of include/jepa_gb300.h
+ABI_VERSION = 6  # JEPA_ABI_VERSION of include/jepa_gb300.h
 
 
 class EncoderParams(C.Structure):
@@ -43,6 +43,11 @@ class PredictorParams(C.Structure):
                 ("in_dim", C.c_int), ("out_dim", C.c_int), ("n_mask_tokens", C.c_int), ("mask_index", C.c_int),
                 ("ln_eps", C.c_float), ("rope_theta", C.c_float), ("rope_layout", C.c_int), ("dtype", C.c_int),
                 ("has_mod_embed", C.c_int), ("has_proj_context", C.c_int)]
+
+
+class HeadParams(C.Structure):
+    _fields_ = [("embed_dim", C.c_int), ("n_layer", C.c_int), ("n_head", C.c_int), ("ffn_dim", C.c_int),
+                ("n_classes", C.c_int), ("ln_eps", C.c_float), ("dtype", C.c_int)]
 
 
 VP, I, F, ST, U64 = C.c_void_p, C.c_int, C.c_float, C.c_int, C.c_size_t
@@ -78,6 +83,11 @@ SIGNATURES = {
     "jepa_ops_sync": (ST, [VP]),
     "jepa_selftest_wait_timeout": (ST, [I, VP]),
     "jepa_patch_embed_static": (ST, [VP, VP, VP, VP, VP, I, I, I, I, I, I, VP]),
+    "jepa_head_blob_check": (ST, [VP, U64, C.POINTER(HeadParams)]),
+    "jepa_head_create": (ST, [VP, U64, C.POINTER(HeadParams), I, C.POINTER(VP)]),
+    "jepa_head_destroy": (None, [VP]),
+    "jepa_head_forward": (ST, [VP, VP, I, I, VP, VP, VP]),
+    "jepa_head_sync": (ST, [VP, VP]),
     "jepa_last_error": (C.c_char_p, []),
     "jepa_abi_version": (C.c_int, []),
 }

@@ -13,7 +13,7 @@ import numpy as np
 import torch
 
 from . import _lib
-from ._lib import EncoderParams, PredictorParams, check, load
+from ._lib import EncoderParams, HeadParams, PredictorParams, check, load
 
 DTYPE_CODE = {"f32": _lib.DT_F32, "f16": _lib.DT_F16, "bf16": _lib.DT_BF16}
 TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
@@ -311,6 +311,70 @@ class Predictor:
 
     def sync(self, stream=None):
         check(self.lib.jepa_predictor_sync(self.handle, _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- attentive-pool head
+def head_tensor_order(hc):
+    """(name, is_matrix) in the head blob order of the ABI header."""
+    names = [("head.query", False)]
+    for i in range(hc.n_layer):
+        p = f"head.blk.{i}."
+        names += [(p + "ln1.weight", False), (p + "ln1.bias", False), (p + "attn_qkv.weight", True),
+                  (p + "attn_qkv.bias", False), (p + "attn_out.weight", True), (p + "attn_out.bias", False),
+                  (p + "ln2.weight", False), (p + "ln2.bias", False), (p + "ffn_up.weight", True),
+                  (p + "ffn_up.bias", False), (p + "ffn_down.weight", True), (p + "ffn_down.bias", False)]
+    x = "head.xattn."
+    names += [(x + "ln_kv.weight", False), (x + "ln_kv.bias", False), (x + "q.weight", True), (x + "q.bias", False),
+              (x + "k.weight", True), (x + "k.bias", False), (x + "v.weight", True), (x + "v.bias", False),
+              (x + "ln2.weight", False), (x + "ln2.bias", False), (x + "ffn_up.weight", True),
+              (x + "ffn_up.bias", False), (x + "ffn_down.weight", True), (x + "ffn_down.bias", False),
+              ("head.cls.weight", True), ("head.cls.bias", False)]
+    return names
+
+
+def head_params(hc, dtype: str) -> HeadParams:
+    p = HeadParams()
+    p.embed_dim, p.n_layer, p.n_head, p.ffn_dim = hc.embed_dim, hc.n_layer, hc.n_head, hc.ffn_dim
+    p.n_classes, p.ln_eps, p.dtype = hc.n_classes, hc.ln_eps, DTYPE_CODE[dtype]
+    return p
+
+
+class Head:
+    """The attentive-pool head and classifier resident on one GPU."""
+
+    def __init__(self, hc, weights: dict, dtype: str, device: int = 0):
+        self.lib = load()
+        self.hc = hc
+        self.params = head_params(hc, dtype)
+        blob = pack_blob(head_tensor_order(hc), weights, dtype)
+        h = C.c_void_p()
+        with torch.cuda.device(device):
+            check(self.lib.jepa_head_create(blob, len(blob), C.byref(self.params), device, C.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.lib.jepa_head_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward(self, tokens: torch.Tensor, pooled: bool = False, stream=None, out=None):
+        """tokens: float [B, N, D] on the device.  Returns logits [B, n_classes]
+        (and pooled [B, D] when asked, as (logits, pooled))."""
+        B, N, _ = tokens.shape
+        logits = out if out is not None else torch.empty((B, self.hc.n_classes), dtype=torch.float32,
+                                                         device=tokens.device)
+        pool = torch.empty((B, self.hc.embed_dim), dtype=torch.float32, device=tokens.device) if pooled else None
+        check(self.lib.jepa_head_forward(self.handle, _ptr(tokens), B, N, _ptr(logits), _ptr(pool), _stream(stream)))
+        return (logits, pool) if pooled else logits
+
+    def sync(self, stream=None):
+        check(self.lib.jepa_head_sync(self.handle, _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- single operations

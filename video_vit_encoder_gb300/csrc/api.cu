@@ -1528,3 +1528,241 @@ jepa_status jepa_selftest_wait_timeout(int timeout_us, void* stream) {
 }
 
 }  // extern "C"
+
+// ============================================================================= attentive-pool head
+struct jepa_head {
+  jepa_head_params p{};
+  int device = 0, sms = 0;
+  void* d_weights = nullptr;
+  const float* query = nullptr;
+  std::vector<Block> blocks;
+  const float *kv_w = nullptr, *kv_b = nullptr;
+  const void *wq = nullptr, *wk = nullptr, *wv = nullptr;
+  const float *bq = nullptr, *bk = nullptr, *bv = nullptr;
+  const float *ln2_w = nullptr, *ln2_b = nullptr;
+  const void *w_up = nullptr, *w_down = nullptr, *w_cls = nullptr;
+  const float *b_up = nullptr, *b_down = nullptr, *b_cls = nullptr;
+  float* q = nullptr;  // [D]    q0 Wq^T + bq (computed at create)
+  float* g = nullptr;  // [H, D] ln_kv's gamma * Wk_h^T q_h / sqrt(hd)
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  int* d_status = nullptr;
+  RopeCache rope;      // the identity rotation (one grid cell): the pool blocks carry no RoPE
+  Profiler prof;
+};
+
+namespace {
+
+constexpr int kHeadChunk = 256;  // tokens per partial weighted sum
+
+std::vector<Expect> expected_head(const jepa_head_params& p) {
+  std::vector<Expect> v;
+  const uint32_t D = p.embed_dim, F = p.ffn_dim, C = p.n_classes;
+  v.push_back({DTYPE_F32, D, 1, 1});                     // head.query
+  for (int i = 0; i < p.n_layer; ++i) push_block(v, p.dtype, D, F);
+  v.push_back({DTYPE_F32, D, 1, 1});                     // xattn.ln_kv
+  v.push_back({DTYPE_F32, D, 1, 1});
+  for (int j = 0; j < 3; ++j) {                          // xattn.q, k, v
+    v.push_back({p.dtype, D, D, 2});
+    v.push_back({DTYPE_F32, D, 1, 1});
+  }
+  v.push_back({DTYPE_F32, D, 1, 1});                     // xattn.ln2
+  v.push_back({DTYPE_F32, D, 1, 1});
+  v.push_back({p.dtype, F, D, 2});                       // xattn.ffn_up
+  v.push_back({DTYPE_F32, F, 1, 1});
+  v.push_back({p.dtype, D, F, 2});                       // xattn.ffn_down
+  v.push_back({DTYPE_F32, D, 1, 1});
+  v.push_back({p.dtype, C, D, 2});                       // cls
+  v.push_back({DTYPE_F32, C, 1, 1});
+  return v;
+}
+
+jepa_status check_head_params(const jepa_head_params* p) {
+  if (p == nullptr) return fail(JEPA_ERR_ARG, "params is NULL");
+  JEPA_TRY(check_width(p->embed_dim, p->n_head, p->ffn_dim, p->dtype, "head"));
+  if (p->embed_dim / p->n_head != 64) return fail(JEPA_ERR_UNSUPPORTED, "head: head_dim must be 64");
+  if (p->embed_dim > 1024) return fail(JEPA_ERR_UNSUPPORTED, "head: embed_dim %d (at most 1024)", p->embed_dim);
+  if (p->n_layer < 0 || p->n_classes < 1) return fail(JEPA_ERR_ARG, "head: n_layer %d, n_classes %d", p->n_layer, p->n_classes);
+  if (!(p->ln_eps > 0.f)) return fail(JEPA_ERR_ARG, "head: ln_eps must be > 0");
+  return JEPA_OK;
+}
+
+// Workspace of one head call: the blocks' Work, then scores [M, H], row
+// statistics [M, 2], softmax weights [B, H, n], partial sums [chunks, B, H,
+// D], z [B, H, D], y [B, D], ln2(y) [B, D], hidden [B, F], pooled [B, D].
+struct HeadWork {
+  Work w;
+  float *s, *stats, *wts, *part, *z, *y, *yn, *hid, *pooled;
+};
+
+size_t head_extra_floats(int B, int n, int D, int F) {
+  const size_t H = D / 64, M = (size_t)B * n, chunks = (n + kHeadChunk - 1) / kHeadChunk;
+  return align256(M * H * 4) + align256(M * 8) + align256((size_t)B * H * n * 4) +
+         align256(chunks * B * H * D * 4) + align256((size_t)B * H * D * 4) + 3 * align256((size_t)B * D * 4) +
+         align256((size_t)B * F * 4);
+}
+
+HeadWork head_carve(void* base, int dtype, int B, int n, int D, int F) {
+  HeadWork hw;
+  hw.w = carve(base, dtype, B, n, D, F, 0, false);
+  const size_t H = D / 64, M = (size_t)B * n, chunks = (n + kHeadChunk - 1) / kHeadChunk;
+  uint8_t* p = static_cast<uint8_t*>(base) + work_bytes(dtype, B, n, D, F, 0, false);
+  hw.s = reinterpret_cast<float*>(p);      p += align256(M * H * 4);
+  hw.stats = reinterpret_cast<float*>(p);  p += align256(M * 8);
+  hw.wts = reinterpret_cast<float*>(p);    p += align256((size_t)B * H * n * 4);
+  hw.part = reinterpret_cast<float*>(p);   p += align256(chunks * B * H * D * 4);
+  hw.z = reinterpret_cast<float*>(p);      p += align256((size_t)B * H * D * 4);
+  hw.y = reinterpret_cast<float*>(p);      p += align256((size_t)B * D * 4);
+  hw.yn = reinterpret_cast<float*>(p);     p += align256((size_t)B * D * 4);
+  hw.pooled = reinterpret_cast<float*>(p); p += align256((size_t)B * D * 4);
+  hw.hid = reinterpret_cast<float*>(p);
+  return hw;
+}
+
+}  // namespace
+
+extern "C" {
+
+jepa_status jepa_head_blob_check(const void* blob, size_t blob_bytes, const jepa_head_params* params) {
+  JEPA_TRY(check_head_params(params));
+  std::vector<BlobEntry> ent;
+  return parse_blob(blob, blob_bytes, expected_head(*params), ent);
+}
+
+jepa_status jepa_head_create(const void* blob, size_t blob_bytes, const jepa_head_params* params, int device,
+                             jepa_head** out) {
+  if (out == nullptr) return fail(JEPA_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  JEPA_TRY(check_head_params(params));
+  std::vector<BlobEntry> ent;
+  JEPA_TRY(parse_blob(blob, blob_bytes, expected_head(*params), ent));
+  CUDA_TRY(cudaSetDevice(device));
+  jepa_head* hd = new jepa_head();
+  hd->p = *params;
+  hd->device = device;
+  cudaDeviceGetAttribute(&hd->sms, cudaDevAttrMultiProcessorCount, device);
+  std::vector<const void*> P;
+  jepa_status st = upload_weights(blob, ent, &hd->d_weights, P);
+  if (st != JEPA_OK) {
+    delete hd;
+    return st;
+  }
+  size_t i = 0;
+  hd->query = (const float*)P[i++];
+  for (int l = 0; l < params->n_layer; ++l) hd->blocks.push_back(take_block(P, i));
+  hd->kv_w = (const float*)P[i++];
+  hd->kv_b = (const float*)P[i++];
+  hd->wq = P[i++];
+  hd->bq = (const float*)P[i++];
+  hd->wk = P[i++];
+  hd->bk = (const float*)P[i++];
+  hd->wv = P[i++];
+  hd->bv = (const float*)P[i++];
+  hd->ln2_w = (const float*)P[i++];
+  hd->ln2_b = (const float*)P[i++];
+  hd->w_up = P[i++];
+  hd->b_up = (const float*)P[i++];
+  hd->w_down = P[i++];
+  hd->b_down = (const float*)P[i++];
+  hd->w_cls = P[i++];
+  hd->b_cls = (const float*)P[i++];
+  const int D = params->embed_dim, H = params->n_head;
+  if (cudaMalloc(&hd->q, D * sizeof(float)) != cudaSuccess ||
+      cudaMalloc(&hd->g, (size_t)H * D * sizeof(float)) != cudaSuccess ||
+      cudaMalloc(&hd->d_status, sizeof(int)) != cudaSuccess) {
+    jepa_head_destroy(hd);
+    return fail(JEPA_ERR_OOM, "head: small allocations failed");
+  }
+  cudaMemset(hd->d_status, 0, sizeof(int));
+  cudaError_t e = head_fold_query(params->dtype, hd->wq, hd->bq, hd->query, hd->wk, hd->kv_w, hd->q, hd->g, D, H, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    jepa_head_destroy(hd);
+    return fail(JEPA_ERR_CUDA, "head create: %s", cudaGetErrorString(e));
+  }
+  // one grid cell: every token at position (0, 0, 0), cos 1 and sin 0 on every pair
+  st = rope_prepare(hd->rope, 64, 0, 10000.f, 1, 1, 1, 0, 0, 0);
+  if (st != JEPA_OK) {
+    jepa_head_destroy(hd);
+    return st;
+  }
+  *out = hd;
+  return JEPA_OK;
+}
+
+void jepa_head_destroy(jepa_head* hd) {
+  if (hd == nullptr) return;
+  cudaSetDevice(hd->device);
+  cudaDeviceSynchronize();
+  cudaFree(hd->d_weights);
+  cudaFree(hd->q);
+  cudaFree(hd->g);
+  cudaFree(hd->ws);
+  cudaFree(hd->d_status);
+  cudaFree(hd->rope.d);
+  delete hd;
+}
+
+jepa_status jepa_head_forward(jepa_head* hd, const float* tokens, int batch, int n_tokens, float* logits,
+                              float* pooled, void* stream) {
+  if (hd == nullptr) return fail(JEPA_ERR_ARG, "head handle is NULL");
+  if (tokens == nullptr || logits == nullptr) return fail(JEPA_ERR_ARG, "tokens and logits are required");
+  if (!aligned16(tokens) || !aligned16(logits) || !aligned16(pooled))
+    return fail(JEPA_ERR_ARG, "device buffers must be 16-byte aligned");
+  if (batch < 1 || n_tokens < 1) return fail(JEPA_ERR_ARG, "batch %d and n_tokens %d must be >= 1", batch, n_tokens);
+  const int D = hd->p.embed_dim, F = hd->p.ffn_dim, H = hd->p.n_head, C = hd->p.n_classes, dt = hd->p.dtype;
+  if ((long long)batch * n_tokens * std::max(3 * D, F) >= (1ll << 31)) return fail(JEPA_ERR_ARG, "too many rows");
+  cudaStream_t s = (cudaStream_t)stream;
+  CUDA_TRY(cudaSetDevice(hd->device));
+  const size_t need = work_bytes(dt, batch, n_tokens, D, F, 0, false) + head_extra_floats(batch, n_tokens, D, F);
+  if (need > hd->ws_bytes) {
+    cudaFree(hd->ws);
+    hd->ws = nullptr;
+    hd->ws_bytes = 0;
+    if (cudaMalloc(&hd->ws, need) != cudaSuccess) return fail(JEPA_ERR_OOM, "head workspace: cudaMalloc(%zu)", need);
+    if (cudaMemset(hd->ws, 0, need) != cudaSuccess) return fail(JEPA_ERR_CUDA, "head workspace memset");
+    hd->ws_bytes = need;
+  }
+  HeadWork hw = head_carve(hd->ws, dt, batch, n_tokens, D, F);
+  const int M = batch * n_tokens;
+  // the pool blocks work in place on a copy of the encoder tokens
+  CUDA_TRY(cudaMemcpyAsync(hw.w.x, tokens, (size_t)M * D * sizeof(float), cudaMemcpyDeviceToDevice, s));
+  StackDesc sd;
+  sd.D = D;
+  sd.H = H;
+  sd.F = F;
+  sd.dtype = dt;
+  sd.eps = hd->p.ln_eps;
+  sd.blocks = &hd->blocks;
+  sd.n_hier = 0;
+  sd.hier_layers = nullptr;
+  sd.hier_w = nullptr;
+  sd.hier_b = nullptr;
+  JEPA_TRY(run_blocks(sd, hw.w, batch, n_tokens, 0, hd->p.n_layer, hd->rope.rp, nullptr, nullptr, hd->d_status,
+                      hd->prof, s, hd->sms));
+  // cross-attention of the learned query over ln_kv(x)
+  JEPA_TRY(cuda_status(head_xattn_scores(hw.w.x, hd->g, hw.s, hw.stats, M, D, hd->p.ln_eps, hd->sms, s), "head scores"));
+  JEPA_TRY(cuda_status(head_xattn_pool(hw.w.x, hw.s, hw.stats, hd->kv_w, hd->kv_b, hw.wts, hw.part, hw.z, batch,
+                                       n_tokens, D, kHeadChunk, s),
+                       "head pooling"));
+  constexpr int kAll = 1 << 30;   // every output column reads the same A row
+  float* pool = pooled != nullptr ? pooled : hw.pooled;
+  // y = q0 + Wv_h z_h + bv (no output projection; the residual is the raw query)
+  JEPA_TRY(cuda_status(head_rowvec(dt, false, hw.z, H * D, 64, D, hd->wv, hd->bv, hd->query, 0, hw.y, D, batch, D, D, s),
+                       "head values"));
+  JEPA_TRY(cuda_status(layernorm(DTYPE_F32, hw.y, hd->ln2_w, hd->ln2_b, hw.yn, batch, D, hd->p.ln_eps, s), "head ln2"));
+  JEPA_TRY(cuda_status(head_rowvec(dt, true, hw.yn, D, kAll, 0, hd->w_up, hd->b_up, nullptr, 0, hw.hid, F, batch, F, D, s),
+                       "head ffn_up"));
+  JEPA_TRY(cuda_status(head_rowvec(dt, false, hw.hid, F, kAll, 0, hd->w_down, hd->b_down, hw.y, D, pool, D, batch, D, F, s),
+                       "head ffn_down"));
+  return cuda_status(head_rowvec(dt, false, pool, D, kAll, 0, hd->w_cls, hd->b_cls, nullptr, 0, logits, C, batch, C, D, s),
+                     "head classifier");
+}
+
+jepa_status jepa_head_sync(jepa_head* hd, void* stream) {
+  if (hd == nullptr) return fail(JEPA_ERR_ARG, "head handle is NULL");
+  CUDA_TRY(cudaSetDevice(hd->device));
+  return read_status(hd->d_status, (cudaStream_t)stream);
+}
+
+}  // extern "C"

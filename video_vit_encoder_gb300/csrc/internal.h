@@ -87,4 +87,21 @@ cudaError_t fill_rows(float* dst, const float* row, int n, int dim, cudaStream_t
 cudaError_t add_row_vector(float* x, const float* v, int rows, int dim, cudaStream_t s);
 cudaError_t wait_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t s);
 
+// Attentive-pool head (head_dim 64, D = 256, 512, 768 or 1024).
+// q_out [D] = Wq q0 + bq; g_out [H, D] = gamma_kv * (Wk_h^T q_h / sqrt(hd)).
+cudaError_t head_fold_query(int dtype, const void* Wq, const float* bq, const float* q0, const void* Wk,
+                            const float* gamma_kv, float* q_out, float* g_out, int D, int H, cudaStream_t s);
+// s [rows, H] scores, stats [rows, 2] = (mean, 1/std) of each row of x [rows, D].
+cudaError_t head_xattn_scores(const float* x, const float* g, float* s, float* stats, int rows, int D, float eps,
+                              int num_sms, cudaStream_t st);
+// z [B, H, D] = gamma * sum_i softmax_i(s[:, h]) rstd_i (x_i - mu_i) + beta per clip;
+// w [B, H, n] and part [ceil(n / chunk), B, H, D] are scratch.
+cudaError_t head_xattn_pool(const float* x, const float* s, const float* stats, const float* gamma,
+                            const float* beta, float* w, float* part, float* z, int B, int n, int D, int chunk,
+                            cudaStream_t st);
+// out[b, n] = act(A[b*lda + (n/group)*gstride + :K] . W[n, :] + bias[n]) + res[b*ldr + n].
+cudaError_t head_rowvec(int dtype, bool gelu, const float* A, int lda, int group, int gstride, const void* W,
+                        const float* bias, const float* res, int ldr, float* out, int ldo, int B, int N, int K,
+                        cudaStream_t s);
+
 }  // namespace jepa

@@ -7,7 +7,8 @@ out_proj_f32 / out_proj_bf16 (the out_proj shape with a plain fp32 or 16-bit
 store instead of the residual add), and predictor21: the whole V-JEPA 2.1
 masked predictor (D 384, 12 blocks, head_dim 32, FFN 1536, out 1664, context
 projection) on a 16-frame 384 px clip's 4608 tokens split 2304 / 2304, random
-encoder tokens and weights.  Encoder-op shapes:
+encoder tokens and weights; head: the SSv2 attentive-pool head and
+classifier (3 pool blocks, 174 classes) on 8 x 2048 random encoder tokens.  Encoder-op shapes:
 8 clips x 2048 tokens = 16384 rows, D 1024, 16 heads (head_dim 64), FFN 4096,
 bf16 operands.  Inputs are random (the values do not matter for timing).
 Prints the mean time per launch (CUDA events) and the achieved rate.  Used
@@ -67,6 +68,18 @@ def _setup(op):
         vt = torch.zeros(B * H, hd, N, dtype=bf, device="cuda")
         return (lambda: jb.qkv_rope(A, W, bias, B, N, H, (8, 16, 16), "tiled", out=(q, k, vt))), \
             2.0 * M * 3 * D * D, "TFLOP/s"
+    if op == "head":
+        # the SSv2 attentive-pool head + classifier on 8 clips x 2048 encoder tokens
+        import synth
+        from . import binding
+        hc = synth.HEAD_SSV2
+        head = binding.Head(hc, synth.head_weights(hc, 2, "bf16"), "bf16")
+        x = torch.randn(B, N, D, device="cuda", generator=g)
+        logits = torch.empty(B, hc.n_classes, device="cuda")
+        F_ = hc.ffn_dim
+        fl = (hc.n_layer * (2 * M * (4 * D * D + 2 * D * F_) + 4 * B * N * N * D)   # pool blocks
+              + 4 * M * D * (D // 64) + 2 * B * (2 * D * D + 2 * D * F_ + hc.n_classes * D))
+        return (lambda: head.forward(x, out=logits)), fl, "TFLOP/s"
     if op == "layernorm":
         x = rnd(M, D, dtype=torch.float32)
         w, b = torch.ones(D, device="cuda"), torch.zeros(D, device="cuda")
@@ -85,7 +98,7 @@ def _setup(op):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("op", choices=["attention", "qkv", "out_proj", "ffn_up", "ffn_down", "layernorm", "out_proj_f32",
-                                   "out_proj_bf16", "predictor21"])
+                                   "out_proj_bf16", "predictor21", "head"])
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args(argv)
