@@ -8,7 +8,9 @@ store instead of the residual add), and predictor21: the whole V-JEPA 2.1
 masked predictor (D 384, 12 blocks, head_dim 32, FFN 1536, out 1664, context
 projection) on a 16-frame 384 px clip's 4608 tokens split 2304 / 2304, random
 encoder tokens and weights; head: the SSv2 attentive-pool head and
-classifier (3 pool blocks, 174 classes) on 8 x 2048 random encoder tokens.  Encoder-op shapes:
+classifier (3 pool blocks, 174 classes) on 8 x 2048 random encoder tokens;
+patch_embed: normalise, unfold and patch-embed GEMM of 8 random 16 x 256 x 256
+uint8 clips.  Encoder-op shapes:
 8 clips x 2048 tokens = 16384 rows, D 1024, 16 heads (head_dim 64), FFN 4096,
 bf16 operands.  Inputs are random (the values do not matter for timing).
 Prints the mean time per launch (CUDA events) and the achieved rate.  Used
@@ -80,6 +82,14 @@ def _setup(op):
         fl = (hc.n_layer * (2 * M * (4 * D * D + 2 * D * F_) + 4 * B * N * N * D)   # pool blocks
               + 4 * M * D * (D // 64) + 2 * B * (2 * D * D + 2 * D * F_ + hc.n_classes * D))
         return (lambda: head.forward(x, out=logits)), fl, "TFLOP/s"
+    if op == "patch_embed":
+        # normalise + tubelet unfold + patch-embed GEMM of 8 clips of 16 x 256 x 256 (jepa_encoder_embed)
+        import synth
+        from . import binding
+        cfg = synth.CONFIGS["c3"].with_(n_layer=0)
+        enc = binding.Encoder(cfg, synth.encoder_weights(cfg))
+        clip = torch.randint(0, 256, (B, 16, 256, 256, 3), dtype=torch.uint8, device="cuda", generator=g)
+        return (lambda: enc.embed(clip)), 2.0 * M * 1536 * D, "TFLOP/s"
     if op == "layernorm":
         x = rnd(M, D, dtype=torch.float32)
         w, b = torch.ones(D, device="cuda"), torch.zeros(D, device="cuda")
@@ -98,7 +108,7 @@ def _setup(op):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("op", choices=["attention", "qkv", "out_proj", "ffn_up", "ffn_down", "layernorm", "out_proj_f32",
-                                   "out_proj_bf16", "predictor21", "head"])
+                                   "out_proj_bf16", "predictor21", "head", "patch_embed"])
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args(argv)
