@@ -486,6 +486,17 @@ __device__ __forceinline__ void rope_apply(float* v, int dim0, const RopeParams&
 // ----------------------------------------------------------------------------- GEMM epilogues
 enum EpiKind : int { EPI_STORE = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_GELU = 3, EPI_QKV = 4 };
 
+// The fused normalisation (px - 255 mean) / (255 std) of the ImageNet
+// statistics ("V-JEPA 2.1 ViT-B/16 384 - HuggingFace port", Preprocessing;
+// "Parity ...", Preprocessing parity), evaluated as (px - 255 mean) * r with
+// r = 1 / (255 std) rounded once to fp32.
+__host__ __device__ constexpr float pix_mean255(int c) {
+  return c == 0 ? 255.0f * 0.485f : (c == 1 ? 255.0f * 0.456f : 255.0f * 0.406f);
+}
+__host__ __device__ constexpr float pix_rcp255(int c) {
+  return c == 0 ? 1.0f / (255.0f * 0.229f) : (c == 1 ? 1.0f / (255.0f * 0.224f) : 1.0f / (255.0f * 0.225f));
+}
+
 struct EpiParams {
   const float* bias;  // [N] or null
   void* out;          // EPI_STORE/GELU: T [M, ldo]; EPI_F32/RESID: float [M, ldo]

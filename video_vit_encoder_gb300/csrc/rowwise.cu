@@ -7,12 +7,12 @@ namespace jepa {
 
 namespace {
 
-// ImageNet statistics ("V-JEPA 2.1 ViT-B/16 384 - HuggingFace port",
-// Preprocessing), applied in the fused form (px - 255 mean) / (255 std) of
-// the jepa.cpp parity report (Preprocessing parity).
-__constant__ float c_mean255[3] = {255.0f * 0.485f, 255.0f * 0.456f, 255.0f * 0.406f};
-__constant__ float c_std255[3] = {255.0f * 0.229f, 255.0f * 0.224f, 255.0f * 0.225f};
 
+// The normalisation is the fused form (px - 255 mean) / (255 std) with the
+// ImageNet statistics, as a product with the reciprocal (pix_mean255 and
+// pix_rcp255 in common.cuh): a division per value made the kernel bound by
+// instruction issue.
+//
 // One thread per (token, dt, y): reads the 16 pixels x 3 channels of one
 // tubelet row (48 contiguous bytes of the THWC clip) and writes the three
 // 16-wide runs c*(TUB*256) + dt*256 + y*16 + [0,16) of the token's
@@ -50,7 +50,7 @@ __global__ void unfold_u8_kernel(const uint8_t* __restrict__ clip, T* __restrict
   for (int c = 0; c < 3; ++c) {
     float v[16];
 #pragma unroll
-    for (int x = 0; x < 16; ++x) v[x] = ((float)px[3 * x + c] - c_mean255[c]) / c_std255[c];
+    for (int x = 0; x < 16; ++x) v[x] = ((float)px[3 * x + c] - pix_mean255(c)) * pix_rcp255(c);
     T* d = dst + c * (TUB * 256);
     if constexpr (sizeof(T) == 2) {
       uint4 u0, u1;
