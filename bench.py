@@ -15,7 +15,8 @@ between timed steps by writing a 256 MB buffer outside the timed region.
 
 --workload vitb16-img384 measures the V-JEPA 2.1 native image path instead
 (ViT-B/16, 32 images of 384 x 384, 576 tokens each) and prints the same line
-for that workload.
+for that workload; --workload vitl16-16f256-ssv2 adds the SSv2 attentive-pool
+head and 174-class classifier to every step.
 
 Under torchrun (N > 1) every rank runs its own replica (weak scaling, no
 collective on the data path); rank 0 prints one JSON line.
@@ -49,6 +50,11 @@ WORKLOADS = {
                       "bf16 tensor peak",
                       "ViT-B/16 12L D768 h12 FFN3072, bf16, 2.1 native image path (tubelet 1, patch_embed_img), "
                       "interleaved interpolated RoPE, 1f x 384x384 (576 tokens/image), batch 32 per GPU", None),
+    "vitl16-16f256-ssv2": ("c3", "classified tokens/sec (ViT-L/16 encoder + SSv2 attentive-pool head and 174-class "
+                           "classifier, 16f 256px, bf16) and % of bf16 tensor peak",
+                           "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 16f x 256x256 (2048 tokens/clip), then the "
+                           "attentive-pool head (3 pool blocks, 16 heads, single-query cross-attention, 174 classes), "
+                           "batch 8 per GPU", None),
     "vitl16-64f256": ("c4", "encoder tokens/sec (ViT-L/16, 64f 256px, bf16) and % of bf16 tensor peak",
                       "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 64f x 256x256 (8192 tokens/clip), "
                       "batch 1 per GPU", None),
@@ -56,6 +62,9 @@ WORKLOADS = {
                       "ViT-B/16 12L D768 h12 FFN3072, bf16, interleaved interpolated RoPE, 64f x 384x384 "
                       "(18432 tokens/clip), batch 1 per GPU", None),
 }
+# Workloads whose step also runs the SSv2 attentive-pool head and classifier
+# on the encoder's output (the conversion notes' classifier checkpoint geometry).
+HEAD_WORKLOADS = {"vitl16-16f256-ssv2"}
 # The oracle holds each head's full score matrix in float64; above this many
 # tokens per clip one of its blocks no longer fits a bounded CPU sample.
 CPU_BASELINE_MAX_TOKENS = 8192
@@ -85,6 +94,18 @@ def flops_per_clip(cfg, n_tok):
     D, L, F = cfg.embed_dim, cfg.n_layer, cfg.ffn_dim
     per_tok_layer = 2 * (3 * D * D + D * D + 2 * D * F) + 4 * n_tok * D
     return n_tok * (L * per_tok_layer + 2 * _patch_k(cfg) * D)
+
+
+def head_flops_per_clip(hc, n_tok):
+    """Algorithmic FLOPs of the attentive-pool head on one clip: the pool blocks
+    like encoder blocks (no patch embed), the cross-attention's k/v projections
+    of every token and its single-query scores and sums, and the per-clip MLP and
+    classifier."""
+    D, F, L, C = hc.embed_dim, hc.ffn_dim, hc.n_layer, hc.n_classes
+    blocks = n_tok * L * (2 * (3 * D * D + D * D + 2 * D * F) + 4 * n_tok * D)
+    xattn = 2 * n_tok * 2 * D * D + 4 * n_tok * D + 2 * D * D
+    tail = 2 * (D * D + 2 * D * F + C * D)
+    return blocks + xattn + tail
 
 
 def class_flops_per_launch(cfg, batch, n_tok):
@@ -206,7 +227,7 @@ def _oracle_blocks(cfg, weights, x, COS, SIN, l0, l1):
     return x
 
 
-def cpu_baseline(cfg, weights, clip, whole=True):
+def cpu_baseline(cfg, weights, clip, whole=True, head=None):
     """The oracle, as it stands, on the host cores: one clip's forward timed
     end to end (patch embed, every block, final norm) when ``whole``; else
     (clips too long for a bounded sample) the patch embed and one block timed
@@ -222,16 +243,19 @@ def cpu_baseline(cfg, weights, clip, whole=True):
     t0 = time.perf_counter()
     x = _oracle_blocks(cfg, weights, x, COS, SIN, 0, n_run)
     t_blocks = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    oracle.layer_norm(x, weights["norm.weight"], weights["norm.bias"], cfg.ln_eps)
-    t_norm = time.perf_counter() - t0
+    t0 = time.perf_counter()   # the final norm (and the head)
+    out = oracle.layer_norm(x, weights["norm.weight"], weights["norm.bias"], cfg.ln_eps)
+    if head is not None:   # whole clips only: the head on the oracle's own tokens
+        import synth
+        oracle.attentive_pool_forward(head, synth.head_weights(head, cfg.seed, cfg.dtype), out)
+    t_tail = time.perf_counter() - t0
     n_tok = x.shape[0]
     if whole:
-        sec = t_embed + t_blocks + t_norm
-        sample = (f"1 clip ({n_tok} tokens): patch embed + {cfg.n_layer} of {cfg.n_layer} blocks + final norm, "
-                  f"timed end to end in float64: {sec:.2f} s")
+        sec = t_embed + t_blocks + t_tail
+        sample = (f"1 clip ({n_tok} tokens): patch embed + {cfg.n_layer} of {cfg.n_layer} blocks + final norm"
+                  f"{' + attentive-pool head' if head is not None else ''}, timed end to end in float64: {sec:.2f} s")
     else:
-        sec = t_embed + cfg.n_layer * t_blocks + t_norm
+        sec = t_embed + cfg.n_layer * t_blocks + t_tail
         sample = (f"1 clip ({n_tok} tokens): patch embed + 1 of {cfg.n_layer} blocks + final norm timed in float64, "
                   f"extrapolated to {cfg.n_layer} blocks: {sec:.2f} s")
     return {"value": n_tok / sec, "unit": UNIT, "cores": blas, "host_cores": host, "kind": "oracle",
@@ -252,8 +276,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     key, metric, workload, keep_frac = WORKLOADS[args.workload]
-    if keep_frac is not None:
-        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the unmasked workloads only"}))
+    if keep_frac is not None or args.workload in HEAD_WORKLOADS:
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the encoder-only unmasked workloads"}))
         return 0
     cfg = synth.CONFIGS[key]
     if synth.tokens_per_clip(cfg) > CPU_BASELINE_MAX_TOKENS:
@@ -344,7 +368,16 @@ def main():
     out = torch.empty((B, n_tok, cfg.embed_dim), dtype=torch.float32, device="cuda")
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
-    if keep_frac is None:
+    head = None
+    if args.workload in HEAD_WORKLOADS:
+        hc = synth.HEAD_SSV2
+        head = jg.Head(hc, synth.head_weights(hc, cfg.seed, cfg.dtype), cfg.dtype, device=local)
+        logits = torch.empty((B, hc.n_classes), dtype=torch.float32, device="cuda")
+
+        def step():
+            enc.encode(clip, out=out)
+            head.forward(out, out=logits)
+    elif keep_frac is None:
         def step():
             enc.encode(clip, out=out)
     else:
@@ -390,6 +423,8 @@ def main():
     tokens = world * B * n_tok * args.steps
     value = tokens / (total_ms / 1e3)
     fl_step = B * flops_per_clip(cfg, n_tok)
+    if head is not None:
+        fl_step += B * head_flops_per_clip(synth.HEAD_SSV2, n_tok)
     peaks = _peaks()
     tflops = fl_step / (ms_step / 1e3) / 1e12
 
@@ -414,8 +449,16 @@ def main():
     hclip = torch.from_numpy(clip_np).pin_memory()
     hout = torch.empty((B, n_tok, cfg.embed_dim), dtype=torch.float32).pin_memory()
 
+    if head is not None:
+        hlogits = torch.empty((B, synth.HEAD_SSV2.n_classes), dtype=torch.float32).pin_memory()
+
     def e2e_serial_step():
-        if keep_frac is None:
+        if head is not None:   # pinned clip in, encoder + head on the device, logits out
+            clip.copy_(hclip, non_blocking=True)
+            step()
+            hlogits.copy_(logits, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        elif keep_frac is None:
             enc.encode_host(hclip, hout)
         else:   # the masked forward has no host entry point: copies around jepa_encode_masked
             clip.copy_(hclip, non_blocking=True)
@@ -437,7 +480,7 @@ def main():
             enc.sync()
         return max_over_ranks((time.perf_counter() - t0) / n, dist, "cuda")
 
-    streaming = keep_frac is None
+    streaming = keep_frac is None and head is None
     e2e_run(2, False)
     if streaming:
         e2e_run(2, True)      # both staging slots and their graphs warm
@@ -459,10 +502,12 @@ def main():
         "kernels": kernels,
         "gpu_launches": gpu_launches,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(hclip.numel()),
-                "d2h_bytes_per_step": int(hout.numel() * 4),
+                "d2h_bytes_per_step": int(hlogits.numel() * 4) if head is not None else int(hout.numel() * 4),
                 "api": "jepa_encode_host_async per step + jepa_encoder_sync at the end (pinned host buffers; "
                        "copies overlap the neighbouring steps' encodes)" if streaming else
-                       "pinned host clip -> device, jepa_encode_masked, device -> pinned host tokens",
+                       ("pinned host clip -> device, jepa_encode + jepa_head_forward, device -> pinned host logits"
+                        if head is not None else
+                        "pinned host clip -> device, jepa_encode_masked, device -> pinned host tokens"),
                 "serial_value": world * B * n_tok / e2e_serial_s,
                 "serial_api": "jepa_encode_host per step (copy in, encode, copy out, synchronise)" if streaming else
                               "as api"},
@@ -479,8 +524,12 @@ def main():
                                               "on the host cores (float64 score matrices)"}
         else:
             # a whole clip up to 2048 tokens (about 17 s for the ViT-L clip); longer clips are extrapolated
-            line["cpu_baseline"] = cpu_baseline(cfg, weights, clip_np[0], whole=synth.tokens_per_clip(cfg) <= 2048)
+            line["cpu_baseline"] = cpu_baseline(cfg, weights, clip_np[0], whole=synth.tokens_per_clip(cfg) <= 2048,
+                                                head=synth.HEAD_SSV2 if head is not None else None)
             line["cpu_baseline"].pop("seconds_per_clip", None)
+    if head is not None:
+        line["config"]["head"] = "SSv2 attentive-pool head: 3 pool blocks, 16 heads, 174 classes"
+        head.close()
     enc.close()
     if rank == 0:
         print(json.dumps(line), flush=True)

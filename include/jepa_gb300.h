@@ -306,6 +306,9 @@ JEPA_API jepa_status jepa_head_forward(jepa_head* head, const float* tokens, int
                                        float* pooled, void* stream);
 /* Synchronises `stream` and reports a device-side timeout of an earlier call. */
 JEPA_API jepa_status jepa_head_sync(jepa_head* head, void* stream);
+/* Replay of repeated jepa_head_forward calls with the same buffers and shapes
+ * as one CUDA graph, as jepa_encoder_set_graphs (on by default). */
+JEPA_API jepa_status jepa_head_set_graphs(jepa_head* head, int on);
 
 /* ---------------------------------------------------------------- single operations
  * The kernels of the encoder, callable one at a time (the same code runs

@@ -108,3 +108,33 @@ def test_ssv2_head_on_vitl_encoder_output(jg):
         ref = oracle.attentive_pool_forward(hc, w, x[b])
         assert_close_16bit(logits[b:b + 1].cpu().numpy(), ref["logits"][None], f"ssv2 logits clip {b}")
         assert_close_16bit(pooled[b:b + 1].cpu().numpy(), ref["pooled"][None], f"ssv2 pooled clip {b}")
+
+
+def test_head_graph_replay_matches_eager(jg):
+    """Repeated calls with the same buffers replay one captured graph (the
+    first eager, the second captured): bit for bit the eager result, also
+    after the tokens' contents change."""
+    w = _weights(HC, "bf16", sharp=True)
+    x = torch.from_numpy(_tokens(2, 200, HC.embed_dim, 9)).cuda()
+    head = jg.Head(HC, w, "bf16")
+    logits = torch.empty(2, HC.n_classes, device="cuda")
+    runs = []
+    for _ in range(3):
+        head.forward(x, out=logits)
+        head.sync()
+        runs.append(logits.clone())
+    head.set_graphs(False)
+    head.forward(x, out=logits)
+    head.sync()
+    for r in runs:
+        assert torch.equal(r, logits)
+    x.copy_(torch.from_numpy(_tokens(2, 200, HC.embed_dim, 10)))
+    head.set_graphs(True)
+    head.forward(x, out=logits)      # replayed on the new contents
+    head.sync()
+    replayed = logits.clone()
+    head.set_graphs(False)
+    head.forward(x, out=logits)
+    head.sync()
+    assert torch.equal(replayed, logits)
+    head.close()

@@ -88,6 +88,7 @@ SIGNATURES = {
     "jepa_head_destroy": (None, [VP]),
     "jepa_head_forward": (ST, [VP, VP, I, I, VP, VP, VP]),
     "jepa_head_sync": (ST, [VP, VP]),
+    "jepa_head_set_graphs": (ST, [VP, I]),
     "jepa_last_error": (C.c_char_p, []),
     "jepa_abi_version": (C.c_int, []),
 }

@@ -376,6 +376,10 @@ class Head:
     def sync(self, stream=None):
         check(self.lib.jepa_head_sync(self.handle, _stream(stream)))
 
+    def set_graphs(self, on: bool):
+        """Replay of repeated forward calls as one CUDA graph (on by default)."""
+        check(self.lib.jepa_head_set_graphs(self.handle, int(bool(on))))
+
 
 # ----------------------------------------------------------------------------- single operations
 def layernorm_f32(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor, eps: float, out=None) -> torch.Tensor:

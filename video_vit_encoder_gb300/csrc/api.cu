@@ -1549,6 +1549,7 @@ struct jepa_head {
   int* d_status = nullptr;
   RopeCache rope;      // the identity rotation (one grid cell): the pool blocks carry no RoPE
   Profiler prof;
+  GraphCache graphs;
 };
 
 namespace {
@@ -1700,6 +1701,7 @@ void jepa_head_destroy(jepa_head* hd) {
   cudaFree(hd->ws);
   cudaFree(hd->d_status);
   cudaFree(hd->rope.d);
+  hd->graphs.release();
   delete hd;
 }
 
@@ -1714,49 +1716,72 @@ jepa_status jepa_head_forward(jepa_head* hd, const float* tokens, int batch, int
   if ((long long)batch * n_tokens * std::max(3 * D, F) >= (1ll << 31)) return fail(JEPA_ERR_ARG, "too many rows");
   cudaStream_t s = (cudaStream_t)stream;
   CUDA_TRY(cudaSetDevice(hd->device));
-  const size_t need = work_bytes(dt, batch, n_tokens, D, F, 0, false) + head_extra_floats(batch, n_tokens, D, F);
-  if (need > hd->ws_bytes) {
+  // workspace (a no-op once sized for this shape)
+  auto prep = [&](cudaStream_t) -> jepa_status {
+    const size_t need = work_bytes(dt, batch, n_tokens, D, F, 0, false) + head_extra_floats(batch, n_tokens, D, F);
+    if (need <= hd->ws_bytes) return JEPA_OK;
     cudaFree(hd->ws);
     hd->ws = nullptr;
     hd->ws_bytes = 0;
     if (cudaMalloc(&hd->ws, need) != cudaSuccess) return fail(JEPA_ERR_OOM, "head workspace: cudaMalloc(%zu)", need);
     if (cudaMemset(hd->ws, 0, need) != cudaSuccess) return fail(JEPA_ERR_CUDA, "head workspace memset");
     hd->ws_bytes = need;
-  }
-  HeadWork hw = head_carve(hd->ws, dt, batch, n_tokens, D, F);
-  const int M = batch * n_tokens;
-  // the pool blocks work in place on a copy of the encoder tokens
-  CUDA_TRY(cudaMemcpyAsync(hw.w.x, tokens, (size_t)M * D * sizeof(float), cudaMemcpyDeviceToDevice, s));
-  StackDesc sd;
-  sd.D = D;
-  sd.H = H;
-  sd.F = F;
-  sd.dtype = dt;
-  sd.eps = hd->p.ln_eps;
-  sd.blocks = &hd->blocks;
-  sd.n_hier = 0;
-  sd.hier_layers = nullptr;
-  sd.hier_w = nullptr;
-  sd.hier_b = nullptr;
-  JEPA_TRY(run_blocks(sd, hw.w, batch, n_tokens, 0, hd->p.n_layer, hd->rope.rp, nullptr, nullptr, hd->d_status,
-                      hd->prof, s, hd->sms));
-  // cross-attention of the learned query over ln_kv(x)
-  JEPA_TRY(cuda_status(head_xattn_scores(hw.w.x, hd->g, hw.s, hw.stats, M, D, hd->p.ln_eps, hd->sms, s), "head scores"));
-  JEPA_TRY(cuda_status(head_xattn_pool(hw.w.x, hw.s, hw.stats, hd->kv_w, hd->kv_b, hw.wts, hw.part, hw.z, batch,
-                                       n_tokens, D, kHeadChunk, s),
-                       "head pooling"));
-  constexpr int kAll = 1 << 30;   // every output column reads the same A row
-  float* pool = pooled != nullptr ? pooled : hw.pooled;
-  // y = q0 + Wv_h z_h + bv (no output projection; the residual is the raw query)
-  JEPA_TRY(cuda_status(head_rowvec(dt, false, hw.z, H * D, 64, D, hd->wv, hd->bv, hd->query, 0, hw.y, D, batch, D, D, s),
-                       "head values"));
-  JEPA_TRY(cuda_status(layernorm(DTYPE_F32, hw.y, hd->ln2_w, hd->ln2_b, hw.yn, batch, D, hd->p.ln_eps, s), "head ln2"));
-  JEPA_TRY(cuda_status(head_rowvec(dt, true, hw.yn, D, kAll, 0, hd->w_up, hd->b_up, nullptr, 0, hw.hid, F, batch, F, D, s),
-                       "head ffn_up"));
-  JEPA_TRY(cuda_status(head_rowvec(dt, false, hw.hid, F, kAll, 0, hd->w_down, hd->b_down, hw.y, D, pool, D, batch, D, F, s),
-                       "head ffn_down"));
-  return cuda_status(head_rowvec(dt, false, pool, D, kAll, 0, hd->w_cls, hd->b_cls, nullptr, 0, logits, C, batch, C, D, s),
-                     "head classifier");
+    return JEPA_OK;
+  };
+  auto body = [&](cudaStream_t st) -> jepa_status {
+    JEPA_TRY(prep(st));
+    HeadWork hw = head_carve(hd->ws, dt, batch, n_tokens, D, F);
+    const int M = batch * n_tokens;
+    // the pool blocks work in place on a copy of the encoder tokens
+    CUDA_TRY(cudaMemcpyAsync(hw.w.x, tokens, (size_t)M * D * sizeof(float), cudaMemcpyDeviceToDevice, st));
+    StackDesc sd;
+    sd.D = D;
+    sd.H = H;
+    sd.F = F;
+    sd.dtype = dt;
+    sd.eps = hd->p.ln_eps;
+    sd.blocks = &hd->blocks;
+    sd.n_hier = 0;
+    sd.hier_layers = nullptr;
+    sd.hier_w = nullptr;
+    sd.hier_b = nullptr;
+    JEPA_TRY(run_blocks(sd, hw.w, batch, n_tokens, 0, hd->p.n_layer, hd->rope.rp, nullptr, nullptr, hd->d_status,
+                        hd->prof, st, hd->sms));
+    // cross-attention of the learned query over ln_kv(x)
+    JEPA_TRY(cuda_status(head_xattn_scores(hw.w.x, hd->g, hw.s, hw.stats, M, D, hd->p.ln_eps, hd->sms, st),
+                         "head scores"));
+    JEPA_TRY(cuda_status(head_xattn_pool(hw.w.x, hw.s, hw.stats, hd->kv_w, hd->kv_b, hw.wts, hw.part, hw.z, batch,
+                                         n_tokens, D, kHeadChunk, st),
+                         "head pooling"));
+    constexpr int kAll = 1 << 30;   // every output column reads the same A row
+    float* pool = pooled != nullptr ? pooled : hw.pooled;
+    // y = q0 + Wv_h z_h + bv (no output projection; the residual is the raw query)
+    JEPA_TRY(cuda_status(head_rowvec(dt, false, hw.z, H * D, 64, D, hd->wv, hd->bv, hd->query, 0, hw.y, D, batch, D,
+                                     D, st),
+                         "head values"));
+    JEPA_TRY(cuda_status(layernorm(DTYPE_F32, hw.y, hd->ln2_w, hd->ln2_b, hw.yn, batch, D, hd->p.ln_eps, st),
+                         "head ln2"));
+    JEPA_TRY(cuda_status(head_rowvec(dt, true, hw.yn, D, kAll, 0, hd->w_up, hd->b_up, nullptr, 0, hw.hid, F, batch,
+                                     F, D, st),
+                         "head ffn_up"));
+    JEPA_TRY(cuda_status(head_rowvec(dt, false, hw.hid, F, kAll, 0, hd->w_down, hd->b_down, hw.y, D, pool, D, batch,
+                                     D, F, st),
+                         "head ffn_down"));
+    return cuda_status(head_rowvec(dt, false, pool, D, kAll, 0, hd->w_cls, hd->b_cls, nullptr, 0, logits, C, batch,
+                                   C, D, st),
+                       "head classifier");
+  };
+  if (!hd->graphs.on) return body(s);
+  // repeated calls with the same buffers and shapes replay one captured graph
+  const uint64_t key[12] = {4, (uint64_t)(uintptr_t)tokens, (uint64_t)batch, (uint64_t)n_tokens,
+                            (uint64_t)(uintptr_t)logits, (uint64_t)(uintptr_t)pooled, 0, 0, 0, 0, 0, 0};
+  return replay(hd->graphs, key, prep, hd->ws, hd->rope.d, body, s);
+}
+
+jepa_status jepa_head_set_graphs(jepa_head* hd, int on) {
+  if (hd == nullptr) return fail(JEPA_ERR_ARG, "head handle is NULL");
+  hd->graphs.on = on != 0;
+  return JEPA_OK;
 }
 
 jepa_status jepa_head_sync(jepa_head* hd, void* stream) {
