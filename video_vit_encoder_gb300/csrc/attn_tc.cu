@@ -50,11 +50,6 @@ static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "regist
 // values per lane), O_t [384 + 64 t, +HD).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
-// Of every four exponent pairs, this many are evaluated by the FMA-pipe
-// polynomial and the rest by ex2.approx.  0: every share measured slower,
-// the exponential loop being bound by instruction issue, not by ex2.
-constexpr int kPolyPairs = 0;
-
 template <int HD, int QBUF>
 struct AttnSmem {
   static constexpr uint32_t kQBytes = kBQ * HD * 2;    // one query tile
@@ -95,35 +90,6 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
-}
-
-// 2^x for two values on the FMA pipe (spares the special-function unit).
-// Range reduction: n = round(x) from the low mantissa bits of x + 1.5*2^23,
-// f = x - n in [-1/2, 1/2]; 2^f by a degree-3 polynomial whose coefficients
-// were fitted here by weighted least squares on Chebyshev nodes of [-1/2, 1/2]
-// (max relative error 7.5e-5, far below the 2^-9 rounding of the 16-bit P);
-// 2^n is added to the exponent field.  x is clamped at -126, where the result
-// is below every value P can still hold next to the row maximum (2^0).
-__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
-  const uint64_t magic = pk2(0x4B400000u, 0x4B400000u);          // 1.5 * 2^23
-  const uint64_t neg_magic = pk2(0xCB400000u, 0xCB400000u);
-  const uint64_t minus1 = pk2(__float_as_uint(-1.0f), __float_as_uint(-1.0f));
-  const uint64_t c3 = pk2(__float_as_uint(0.0551716648042202f), __float_as_uint(0.0551716648042202f));
-  const uint64_t c2 = pk2(__float_as_uint(0.2426111251115799f), __float_as_uint(0.2426111251115799f));
-  const uint64_t c1 = pk2(__float_as_uint(0.6932609677314758f), __float_as_uint(0.6932609677314758f));
-  const uint64_t c0 = pk2(__float_as_uint(0.9999280571937561f), __float_as_uint(0.9999280571937561f));
-  float a, b;
-  upk2(x2, a, b);
-  x2 = pk2(__float_as_uint(fmaxf(a, -126.0f)), __float_as_uint(fmaxf(b, -126.0f)));
-  const uint64_t t = add2(x2, magic);          // 1.5*2^23 + n
-  const uint64_t f = fma2(add2(t, neg_magic), minus1, x2);   // x - n
-  uint64_t p = fma2(f, c3, c2);
-  p = fma2(f, p, c1);
-  p = fma2(f, p, c0);
-  uint32_t tl, th, pl, ph;
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(tl), "=r"(th) : "l"(t));
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(pl), "=r"(ph) : "l"(p));
-  return pk2(pl + (tl << 23), ph + (th << 23));
 }
 
 // Row max of one S tile held in registers (s[c][i] = column 32 c + i);
@@ -171,13 +137,7 @@ __device__ __forceinline__ float exp_to_tmem(const uint32_t (&s)[kBKV / 32][32],
           x0 = col < kvalid ? x0 : -INFINITY;
           x1 = col + 1 < kvalid ? x1 : -INFINITY;
         }
-        float p0, p1;
-        if (!MASK && ((i >> 1) & 3) >= 4 - kPolyPairs) {
-          upk2(exp2_poly2(x2), p0, p1);   // this share of the pairs on the FMA pipe
-        } else {
-          p0 = ex2(x0);
-          p1 = ex2(x1);
-        }
+        const float p0 = ex2(x0), p1 = ex2(x1);
         rs2[(i >> 1) & 3] = add2(rs2[(i >> 1) & 3], pk2(__float_as_uint(p0), __float_as_uint(p1)));
         w[cc * 16 + i / 2] = pack2<T>(p0, p1);
       }

@@ -45,14 +45,6 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) 
   __half2 v = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-template <typename T> __device__ __forceinline__ float2 unpack2(uint32_t u);
-template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t u) {
-  return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
-}
-template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t u) {
-  return __half22float2(*reinterpret_cast<__half2*>(&u));
-}
-
 // Exact-erf GELU, 0.5 z (1 + erf(z / sqrt 2)).
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 
@@ -117,12 +109,6 @@ __device__ __forceinline__ void gelu_as2(float& z0, float& z1) {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // ----------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -290,43 +276,13 @@ __device__ __forceinline__ void tmem_relinquish_pair() {
 __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-// D (+)= A * B^T over the CTA pair (issued by the even CTA): M = 256 rows, A's
-// rows 0-127 and D's lanes in the even CTA, rows 128-255 in the odd one; B's
-// N rows split in halves the same way; the descriptors give the per-CTA
-// shared-memory tiles (same offsets in both CTAs).
-__device__ __forceinline__ void umma_f16_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 or fp16 inputs, fp32 accumulator).
-__device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A (M rows = TMEM lanes, K
-// 16-bit values packed two per 32-bit column, even index in the low half)
-// read from tensor memory at a_tmem.
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Warp-wide forms of the issue calls above: every lane of a converged warp
-// calls them with the same operands and one elected lane issues.  Keeping
+// MMA issue, warp-wide: every lane of a converged warp calls these with the
+// same operands and one elected lane issues.  kind::f16 (bf16 or fp16
+// inputs, fp32 accumulator); _ss: A and B from shared memory, _ts: A from
+// tensor memory (M rows = TMEM lanes, K 16-bit values packed two per 32-bit
+// column, even index in the low half); _pair: over the CTA pair, issued by
+// the even CTA (M = 256 rows, A's rows 0-127 and D's lanes in the even CTA,
+// rows 128-255 in the odd one, B's rows split the same way).  Keeping
 // the whole warp on the issue path lets the operands stay in uniform
 // registers; issued from a single divergent lane, each tcgen05.mma costs
 // about as many cycles as a 128 x 128 x 16 product takes to execute.
@@ -375,11 +331,6 @@ __device__ __forceinline__ void umma_commit_pair_warp(uint64_t* bar, uint16_t ct
           smem_u32(bar)),
       "h"(cta_mask)
       : "memory");
-}
-// Arrives once on `bar` when all tcgen05 operations issued so far by this thread complete.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }

@@ -84,7 +84,6 @@ cudaError_t gather_rows_cast(int dtype, const float* src, int n_src, const int* 
 // Sets DEV_BAD_INDEX in *status when any of the n ids lies outside [0, limit).
 cudaError_t check_ids(const int* ids, long n, int limit, int* status, cudaStream_t s);
 cudaError_t fill_rows(float* dst, const float* row, int n, int dim, cudaStream_t s);
-cudaError_t add_row_vector(float* x, const float* v, int rows, int dim, cudaStream_t s);
 cudaError_t wait_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t s);
 
 // Attentive-pool head (head_dim 64, D = 256, 512, 768 or 1024).
