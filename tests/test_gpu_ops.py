@@ -135,6 +135,15 @@ def _attn_inputs(rng, B, H, N, hd, dtype, logit_std):
     return q, k, v
 
 
+def _plant_lift(q, k, row, key, hd, dtype, lift):
+    """k[:, key] = a multiple of q[:, row] whose logit is `lift` above the
+    row's largest logit over key tile 0 (keys 0-127), per (clip, head)."""
+    scale = 1.0 / math.sqrt(hd)
+    m0 = (np.einsum("bd,bkd->bk", q[:, row], k[:, :128]) * scale).max(1)
+    qq = (q[:, row] ** 2).sum(1) * scale
+    k[:, key] = synth.round_to_dtype(q[:, row] * ((m0 + lift) / qq)[:, None], dtype)
+
+
 def _run_attn(jg, q, k, v, B, H, N, hd, dtype):
     ldv = (N + 7) // 8 * 8
     vt = np.zeros((B * H, hd, ldv))
@@ -160,6 +169,12 @@ def test_attention_tc(jg, dtype, hd, N, logit_std):
         # late and exercises the rescale of the partial output
         k[:, 7] = synth.round_to_dtype(q[:, 3] * 3, dtype)
         k[:, N - 5] = synth.round_to_dtype(q[:, 130] * 3, dtype)
+        # moderate ones in key tile 1: query 250's max grows there by ~2^33
+        # (in the exponent; within bf16's range, beyond fp16's), query 260's
+        # by ~2^11.5 (more than 2^8, within both 16-bit P ranges), so its
+        # running max moves only before key tile 2
+        k[:, 150] = synth.round_to_dtype(q[:, 250], dtype)
+        _plant_lift(q, k, 260, 160, hd, dtype, 8.0)
     got = _run_attn(jg, q, k, v, B, H, N, hd, dtype)
     ref = oracle.attention_heads(q, k, v).reshape(B, H, N, hd).transpose(0, 2, 1, 3).reshape(B, N, H * hd)
     assert_close_16bit(got, ref, f"attention {dtype} hd{hd} N{N}")
@@ -177,6 +192,8 @@ def test_attention_tc_many_units_per_cta(jg, N):
     q, k, v = _attn_inputs(rng, B, H, N, hd, dtype, 4.0)
     k[:, 7] = synth.round_to_dtype(q[:, 3] * 3, dtype)
     k[:, N - 5] = synth.round_to_dtype(q[:, 130] * 3, dtype)
+    k[:, 150] = synth.round_to_dtype(q[:, 250], dtype)
+    _plant_lift(q, k, 260, 160, hd, dtype, 8.0)
     got = _run_attn(jg, q, k, v, B, H, N, hd, dtype)
     ref = oracle.attention_heads(q, k, v).reshape(B, H, N, hd).transpose(0, 2, 1, 3).reshape(B, N, H * hd)
     assert_close_16bit(got, ref, f"attention many units N{N}")
@@ -189,14 +206,18 @@ def test_attention_tc_long_sampled_rows(jg, N, hd, logit_std):
     64-frame 256 px clip with its hd-32 predictor (8192) and the 64-frame
     384 px clip (18 432), bf16.  Sampled query rows are checked against the
     oracle over all keys.  Planted outliers put one row's largest logit in
-    the first key tile and another's in the last key tile."""
+    the first key tile and another's in the last key tile; two rows' maxima
+    grow in key tile 1, far beyond and a little beyond 2^8 (in the
+    exponent)."""
     B, H, dtype = 1, 2, "bf16"
     rng = np.random.default_rng(N * 7 + hd + int(logit_std))
     q, k, v = _attn_inputs(rng, B, H, N, hd, dtype, logit_std)
     k[:, 11] = synth.round_to_dtype(q[:, 5] * 3, dtype)
     k[:, N - 3] = synth.round_to_dtype(q[:, N // 2] * 3, dtype)
+    k[:, 200] = synth.round_to_dtype(q[:, N // 3], dtype)
+    _plant_lift(q, k, N // 4, 210, hd, dtype, 8.0)
     got = _run_attn(jg, q, k, v, B, H, N, hd, dtype).reshape(N, H, hd)
-    rows = np.unique(np.concatenate([[0, 5, N // 2, N - 1], rng.choice(N, 60, replace=False)]))
+    rows = np.unique(np.concatenate([[0, 5, N // 4, N // 3, N // 2, N - 1], rng.choice(N, 60, replace=False)]))
     ref = oracle.attention_heads(q[:, rows], k, v)                  # [H, rows, hd]
     assert_close_16bit(got[rows].transpose(1, 0, 2), ref, f"attention N{N} hd{hd} std{logit_std}")
 
