@@ -155,11 +155,12 @@ def _run_attn(jg, q, k, v, B, H, N, hd, dtype):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("hd", [64, 32])
-@pytest.mark.parametrize("N,logit_std", [(200, 1.0), (384, 4.0), (1000, 1.0), (128, 0.3), (1500, 4.0)])
+@pytest.mark.parametrize("N,logit_std", [(200, 1.0), (384, 4.0), (1000, 1.0), (128, 0.3), (1500, 4.0), (2100, 4.0)])
 def test_attention_tc(jg, dtype, hd, N, logit_std):
-    """Every row against the oracle.  Up to 8 key tiles (1024 tokens) run on
-    the persistent kernel, longer sequences (1500: 12 key tiles, a ragged
-    last one) on the one-unit-per-CTA kernel."""
+    """Every row against the oracle.  Up to 16 key tiles (2048 tokens; 1500:
+    12 key tiles, a ragged last one) run on the persistent kernel, longer
+    sequences (2100: 17 key tiles, a ragged last one) on the one-unit-per-CTA
+    kernel."""
     B, H = 2, 3
     rng = np.random.default_rng(N + hd)
     q, k, v = _attn_inputs(rng, B, H, N, hd, dtype, logit_std)

@@ -2,11 +2,13 @@
 //
 // A work unit is two 128-row query tiles (Q0, Q1) of one (clip, head); keys
 // and values stream in tiles of 128 through a 4-deep TMA ring shared by both
-// query tiles.  Two launch forms: for short sequences the CTAs are persistent
-// (one per SM, taking units in turn, the ring running on across units and Q
-// double-buffered, so one unit's last key tiles overlap the next unit's Q
-// load and first score products); for longer ones each CTA takes one unit on
-// a grid over the units.  For query tile t and key tile j:
+// query tiles.  Two launch forms: for up to 16 key tiles the CTAs are
+// persistent (one per SM, taking units in turn, the ring running on across
+// units and Q double-buffered, so one unit's last key tiles overlap the next
+// unit's Q load and first score products; a unit's output is staged in its
+// own Q buffer and leaves by TMA tile stores, taken at the next unit's first
+// key tile); for longer ones each CTA takes one unit on a grid over the
+// units.  For query tile t and key tile j:
 //   S_t = Q_t K_j^T     tcgen05.mma (both operands in shared memory) into the
 //                       tile's TMEM score buffer (fp32, 128 lanes x 128 columns);
 //   softmax warpgroup t (one thread per query row) reads its row of S_t into
@@ -147,6 +149,44 @@ __device__ __forceinline__ float exp_to_tmem(const uint32_t (&s)[kBKV / 32][32],
   float a, b;
   upk2(add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3])), a, b);
   return a + b;
+}
+
+// This warp's 32 rows of O_t (HD fp32 columns from tO) scaled by inv and
+// rounded to T, into shared memory at stage: 32 rows of 2 HD bytes laid out
+// as a TMA tile with the swizzle of that row width (the 16-byte chunk c of
+// row r at chunk c ^ (bits 7.. of the byte offset)), for one tile store.
+template <typename T, int HD>
+__device__ __forceinline__ void stage_o_rows(uint32_t tO, float inv, uint8_t* stage, int lane) {
+  constexpr uint32_t kRow = HD * 2;          // bytes per row: 128 or 64
+  constexpr uint32_t kMask = kRow / 16 - 1;  // 7 (128-byte swizzle) or 3 (64-byte)
+#pragma unroll
+  for (int c = 0; c < HD / 8; ++c) {  // 8 columns (one 16-byte chunk) at a time
+    uint32_t u[8];
+    tmem_ld8(tO + c * 8, u);
+    tmem_wait_ld();
+    uint4 w;
+    w.x = pack2<T>(__uint_as_float(u[0]) * inv, __uint_as_float(u[1]) * inv);
+    w.y = pack2<T>(__uint_as_float(u[2]) * inv, __uint_as_float(u[3]) * inv);
+    w.z = pack2<T>(__uint_as_float(u[4]) * inv, __uint_as_float(u[5]) * inv);
+    w.w = pack2<T>(__uint_as_float(u[6]) * inv, __uint_as_float(u[7]) * inv);
+    const uint32_t a = (uint32_t)lane * kRow + (uint32_t)c * 16;
+    *reinterpret_cast<uint4*>(stage + (a ^ (((a >> 7) & kMask) << 4))) = w;
+  }
+}
+
+// Stages this warp's 32 rows of O_t (normalised by 1 / l_fin) at stage and
+// has lane 0 store them as one TMA tile: rows row0.., columns head HD.. of
+// clip b of the output.
+template <typename T, int HD>
+__device__ __forceinline__ void store_o_rows(const CUtensorMap* tmO, uint32_t tO, float l_fin, uint8_t* stage,
+                                             int lane, int head, int row0, int b) {
+  stage_o_rows<T, HD>(tO, 1.0f / l_fin, stage, lane);
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_3d(tmO, stage, head * HD, row0, b);
+    bulk_commit_group();
+  }
 }
 
 // One unit (two query tiles of one (clip, head)) per CTA, on a grid over
@@ -415,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <typename T, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                              const __grid_constant__ CUtensorMap tmV, T* __restrict__ out, int n_head, int n_tok,
-                              int n_units, float scale_log2, int* status) {
+                              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                              int n_head, int n_tok, int n_units, float scale_log2, int* status) {
   using S = AttnSmem<HD, 2>;
   constexpr int kQKRow = HD * 2;  // bytes per Q/K row = swizzle width (128 or 64)
   extern __shared__ uint8_t smem_raw[];
@@ -435,7 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pv_done = p_full + 2;         // [2] O_t += P_t V done
   uint64_t* mma_done = pv_done + 2;      // [2] per issuer
   uint64_t* exp_tok = mma_done + 2;      // [2][4] exponential phase of tile t done, per TMEM quarter
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(exp_tok + 8);
+  uint64_t* o_staged = exp_tok + 8;      // [2] Q buffer b's output staging read by its tile stores
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_staged + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -468,11 +509,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&mma_done[0], 1);
     mbar_init(&mma_done[1], 1);
     for (int i = 0; i < 8; ++i) mbar_init(&exp_tok[i], 32);
+    mbar_init(&o_staged[0], 8);  // lane 0 of each softmax warp
+    mbar_init(&o_staged[1], 8);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -497,8 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int u = (int)blockIdx.x + k * (int)gridDim.x;
           const int ubh = u / n_qp, uq0 = (u - ubh * n_qp) * 2 * kBQ;
           const int qb = k & 1;
-          // Q buffer qb was last read by the score products of unit k - 2
-          if (k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) - 1) & 1)) {
+          // Q buffer qb was last read by the score products of unit k - 2,
+          // then held unit k - 2's output on its way to global memory
+          if (k >= 2 && (!mbar_wait(&q_empty[qb], ((k >> 1) - 1) & 1) ||
+                         !mbar_wait(&o_staged[qb], ((k >> 1) - 1) & 1))) {
             ok = false;
             break;
           }
@@ -619,11 +665,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + kColS + t * kBKV;
     const uint32_t tP = tmem + lane_off + kColP + t * 64;
     const uint32_t tO = tmem + lane_off + kColO + t * 64;
+    // A unit's output leaves through its own Q buffer (tile t's half, this
+    // warp's 32 rows), no longer read once the unit's last P V is done: the
+    // warp stages its rows there and lane 0 stores them with one TMA tile
+    // store, so the next unit's first key tile is not held up by global
+    // stores.  The previous unit's output is taken at the next unit's first
+    // key tile, after that tile's score load and row max.
     bool ok = true;
+    bool staged = false;  // the previous unit's rows are staged and their store not yet known to have read them
+    float l_prev = 0.f;
     int g = 0;  // the CTA's key-tile counter over its units
     for (int k = 0; ok && k < n_my; ++k) {
-      const int u = (int)blockIdx.x + k * (int)gridDim.x;
-      const int ubh = u / n_qp, uq0 = (u - ubh * n_qp) * 2 * kBQ;
       float m = -INFINITY;  // running max of the raw scores
       float l = 0.f;
       for (int j = 0; j < n_kv; ++j, ++g) {
@@ -647,10 +699,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mx = full_tile ? row_max<false>(sv, kvalid) : row_max<true>(sv, kvalid);
         if (j == 0) m = mx;
         // O_t is stable and P_t's buffer free once PV_t of the previous key
-        // tile is done (for a unit's first key tile that wait came before the
-        // previous unit's output).
-        if (j >= 1 && !mbar_wait(&pv_done[t], (g - 1) & 1)) ok = false;
+        // tile is done (at a unit's first key tile: the previous unit's last).
+        if (g >= 1 && !mbar_wait(&pv_done[t], (g - 1) & 1)) ok = false;
         tc_fence_after();
+        if (j == 0 && k >= 1) {  // the previous unit's output, before this unit's first P V replaces O_t
+          const int pu = (int)blockIdx.x + (k - 1) * (int)gridDim.x;
+          const int pbh = pu / n_qp, pq0 = (pu - pbh * n_qp) * 2 * kBQ;
+          store_o_rows<T, HD>(&tmO, tO, l_prev,
+                              sQ + ((k - 1) & 1) * 2 * S::kQBytes + t * S::kQBytes + quarter * 32 * kQKRow, lane,
+                              pbh % n_head, pq0 + t * kBQ + quarter * 32, pbh / n_head);
+          staged = true;
+        }
         // Move the running max of the warp's rows when any grew by more than 2^8
         // (in the exponent): O_t and l are rescaled by 2^((m_old - m_new) scale log2e).
         if (__any_sync(0xffffffffu, j > 0 && (mx - m) * scale_log2 > 8.0f)) {
@@ -684,43 +743,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
+        // The staging of the previous unit's rows is released to the
+        // producer (which reloads that Q buffer two units on) a few key
+        // tiles later, when the store has long read it.
+        if (staged && (j == 2 || j == n_kv - 1)) {
+          if (lane == 0) {
+            bulk_wait_read_all();
+            mbar_arrive(&o_staged[(k - 1) & 1]);
+          }
+          staged = false;
+        }
         if (__any_sync(0xffffffffu, !ok)) break;
       }
-      // the unit's last PV (its commit follows every earlier MMA of the issuer)
-      if (ok) ok = mbar_wait(&pv_done[t], (g - 1) & 1);
-      if (__any_sync(0xffffffffu, !ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int row = uq0 + t * kBQ + quarter * 32 + lane;
-      const float inv = 1.0f / l;
-      const int b = ubh / n_head, head = ubh - (ubh / n_head) * n_head;
-      T* op = out + ((size_t)b * n_tok + row) * (size_t)(n_head * HD) + head * HD;
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        uint32_t uo[32];
-        tmem_ld32(tO + c * 32, uo);
-        tmem_wait_ld();
-        if (row < n_tok) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 w;
-            w.x = pack2<T>(__uint_as_float(uo[8 * i + 0]) * inv, __uint_as_float(uo[8 * i + 1]) * inv);
-            w.y = pack2<T>(__uint_as_float(uo[8 * i + 2]) * inv, __uint_as_float(uo[8 * i + 3]) * inv);
-            w.z = pack2<T>(__uint_as_float(uo[8 * i + 4]) * inv, __uint_as_float(uo[8 * i + 5]) * inv);
-            w.w = pack2<T>(__uint_as_float(uo[8 * i + 6]) * inv, __uint_as_float(uo[8 * i + 7]) * inv);
-            reinterpret_cast<uint4*>(op + c * 32)[i] = w;
-          }
-        }
-      }
-      // The next unit's first P (and so its first PV, which starts O_t afresh)
-      // is signalled after these reads, behind the same fence.
+      l_prev = l;
     }
-    if (!ok) {
+    // the last unit's output, once its last P V is done
+    if (ok && n_my > 0) ok = mbar_wait(&pv_done[t], (g - 1) & 1);
+    if (__any_sync(0xffffffffu, !ok)) {
       if (lane == 0) atomicOr(status, DEV_TIMEOUT);
       *abort_flag = 1;
+    } else if (n_my > 0) {
+      tc_fence_after();
+      const int pu = (int)blockIdx.x + (n_my - 1) * (int)gridDim.x;
+      const int pbh = pu / n_qp, pq0 = (pu - pbh * n_qp) * 2 * kBQ;
+      store_o_rows<T, HD>(&tmO, tO, l_prev,
+                          sQ + ((n_my - 1) & 1) * 2 * S::kQBytes + t * S::kQBytes + quarter * 32 * kQKRow, lane,
+                          pbh % n_head, pq0 + t * kBQ + quarter * 32, pbh / n_head);
     }
+    // the CTA does not exit with tile stores in flight
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -733,10 +784,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Sequences of at most this many key tiles run on the persistent kernel:
 // there each unit is short, and overlapping its start with the previous
-// unit's end pays (576-token images: 1.06 -> 0.92 ms per step).  Longer units
-// run one per CTA: the hardware's dynamic hand-out of CTAs balances them
-// better than a fixed round-robin (8192 and 18432 tokens: 9-10 % faster).
-constexpr int kPersistentMaxKeyTiles = 8;
+// unit's end pays (576-token images: 1.06 -> 0.84 ms per step; 2048 tokens:
+// 152.7 -> 149.9 us per ViT-L launch).  Longer units run one per CTA: the
+// hardware's dynamic hand-out of CTAs balances them better than a fixed
+// round-robin (8192 and 18432 tokens: 9-10 % faster).
+constexpr int kPersistentMaxKeyTiles = 16;
 
 template <typename Kern>
 cudaError_t configure(Kern kern, size_t smem_bytes) {
@@ -780,12 +832,18 @@ cudaError_t launch_t(const void* q, const void* k, const void* vt, void* out, in
   static DeviceOnce setup;
   e = setup.run([&](int) { return configure(kern, S::kBytes); });
   if (e != cudaSuccess) return e;
+  // output [batch, n_tok, n_head HD] as 32-row tiles of one head (rows past
+  // n_tok fall outside the map and are not written)
+  CUtensorMap to;
+  e = make_tmap_3d(&to, out, 2, (uint64_t)n_head * HD, n_tok, batch, (uint64_t)n_head * HD * 2,
+                   (uint64_t)n_tok * n_head * HD * 2, HD, 32, 1);
+  if (e != cudaSuccess) return e;
   // persistent grid: one CTA per SM (its shared memory allows no second), each
   // taking every gridDim-th unit
   const int n_units = (int)(n_qp * BH);
   const int slots = num_sms > 0 ? num_sms : 1;
   const int grid = n_units < slots ? n_units : slots;
-  kern<<<grid, kThreads, S::kBytes, s>>>(tq, tk, tv, (T*)out, n_head, n_tok, n_units, scale_log2, status);
+  kern<<<grid, kThreads, S::kBytes, s>>>(tq, tk, tv, to, n_head, n_tok, n_units, scale_log2, status);
   return cudaGetLastError();
 }
 
