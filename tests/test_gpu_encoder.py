@@ -35,6 +35,11 @@ SMALL = {
                                                 width=128, batch=3, hier_layers=(0, 2)),
     "img21-f16": synth.CONFIGS["img384"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=2, height=176,
                                                width=80, batch=2, dtype="f16", hier_layers=(1,)),
+    # the smallest clips: one token (2 frames of 16 x 16), and two tokens along t
+    "v2-1tok": synth.CONFIGS["c3"].with_(embed_dim=256, n_head=4, ffn_dim=512, n_layer=2, n_frames=2,
+                                         height=16, width=16, batch=3),
+    "v2-2tok": synth.CONFIGS["c3"].with_(embed_dim=256, n_head=4, ffn_dim=512, n_layer=2, n_frames=4,
+                                         height=16, width=16, batch=2),
 }
 
 

@@ -181,6 +181,23 @@ def test_attention_tc(jg, dtype, hd, N, logit_std):
     assert_close_16bit(got, ref, f"attention {dtype} hd{hd} N{N}")
 
 
+@pytest.mark.parametrize("hd", [64, 32])
+@pytest.mark.parametrize("N", [1, 2, 7, 127, 129, 255, 257])
+def test_attention_tc_tiny_and_tile_edges(jg, hd, N):
+    """Every row against the oracle at lengths around the tile sizes: one
+    token (the output is v), two, fewer than one 16-byte row of V^T, one
+    short of and one past a 128-key tile, one short of and one past a
+    256-row query-tile pair."""
+    B, H, dtype = 2, 3, "bf16"
+    rng = np.random.default_rng(N * 3 + hd)
+    q, k, v = _attn_inputs(rng, B, H, N, hd, dtype, 2.0)
+    got = _run_attn(jg, q, k, v, B, H, N, hd, dtype)
+    ref = oracle.attention_heads(q, k, v).reshape(B, H, N, hd).transpose(0, 2, 1, 3).reshape(B, N, H * hd)
+    assert_close_16bit(got, ref, f"attention N{N} hd{hd}")
+    if N == 1:
+        np.testing.assert_allclose(got.reshape(B, H, hd), v.reshape(B, H, hd), rtol=0, atol=1e-2)
+
+
 @pytest.mark.parametrize("N", [300, 384])
 def test_attention_tc_many_units_per_cta(jg, N):
     """8 clips x 16 heads give 256 units of two query tiles, more than there
