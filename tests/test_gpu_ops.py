@@ -100,6 +100,28 @@ def test_linear(jg, dtype, epi, M, N, K):
         assert_close_16bit(got, ref, f"linear {dtype} epi {epi}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3])
+@pytest.mark.parametrize("M,N,K", [(1, 32, 64), (3, 96, 64), (129, 160, 192), (300, 224, 128)])
+def test_linear_ragged_width_and_tiny(jg, dtype, epi, M, N, K):
+    """Output widths that leave the last 128-column tile partly (96, 160,
+    224 columns) or mostly (32) outside the output, with a bias of exactly N
+    values; one and three rows; a single K block."""
+    rng = np.random.default_rng(M * 7 + N + K + epi)
+    A = _rounded(rng, (M, K), dtype)
+    W = _rounded(rng, (N, K), dtype, 0.05)
+    b = rng.standard_normal(N).astype(np.float32).astype(np.float64) * 0.1
+    resid = rng.standard_normal((M, N)).astype(np.float32).astype(np.float64)
+    out = _dev(resid) if epi == 2 else None
+    got = jg.linear(_dev(A, dtype), _dev(W, dtype), _dev(b), epi, out=out).float().cpu().numpy()
+    ref = _linear_ref(A, W, b, epi, resid)
+    if dtype == "f32" or epi in (1, 2):
+        m = metrics(got, ref)
+        assert m["rel_max"] <= (1e-5 if dtype == "f32" else 1e-4), (dtype, epi, m)
+    else:
+        assert_close_16bit(got, ref, f"linear {dtype} epi {epi} M{M} N{N}")
+
+
 @pytest.mark.parametrize("epi", [1, 2, 3])
 def test_linear_split_tail_wave(jg, epi):
     """16384 x 1024 outputs are 256 tiles of 256 x 256 for 76 resident CTA
