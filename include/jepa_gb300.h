@@ -131,7 +131,11 @@ JEPA_API jepa_status jepa_predictor_blob_check(const void* blob, size_t blob_byt
 /* ---------------------------------------------------------------- encoder
  * jepa_encoder_create: validates params and the host blob, makes `device`
  * current, copies the weights to device memory (owned by the handle until
- * jepa_encoder_destroy).  The blob may be freed after the call. */
+ * jepa_encoder_destroy).  The blob may be freed after the call.  Supported
+ * widths (JEPA_ERR_UNSUPPORTED otherwise): embed_dim a multiple of 128 (at
+ * most 4096) with head_dim 32 or 64; ffn_dim a multiple of 128 (64 for F32);
+ * the same for the predictor and the head, and a predictor out_dim a
+ * multiple of 128 (32 for F32). */
 typedef struct jepa_encoder jepa_encoder;
 JEPA_API jepa_status jepa_encoder_create(const void* blob, size_t blob_bytes, const jepa_encoder_params* params,
                                 int device, jepa_encoder** out);
@@ -345,8 +349,8 @@ JEPA_API jepa_status jepa_attention(const void* q, const void* k, const void* vt
  *            1: out float [M, N] = acc + bias
  *            2: out float [M, N] += acc + bias   (residual add in place)
  *            3: out dtype [M, N] = gelu_erf(acc + bias)
- * F16/BF16 (tensor cores): K % 64 == 0, N % 32 == 0.  F32: K % 16 == 0,
- * N % 4 == 0. */
+ * F16/BF16 (tensor cores): K % 64 == 0, N % 128 == 0 (whole 128-column
+ * output tiles; JEPA_ERR_ARG otherwise).  F32: K % 16 == 0, N % 4 == 0. */
 JEPA_API jepa_status jepa_linear(const void* A, const void* W, const float* bias, void* out, int M, int N, int K, int dtype,
                         int epilogue, void* stream);
 

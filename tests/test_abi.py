@@ -113,6 +113,8 @@ def test_argument_errors_without_gpu(lib):
     assert lib.jepa_rope3d_f32(C.c_void_p(16), 1, 10, 1, 48, 1, 2, 5, 0, 0, 16, 1e4, None) == ERR_UNSUPPORTED
     assert lib.jepa_rope3d_f32(C.c_void_p(16), 1, 11, 1, 64, 1, 2, 5, 0, 0, 16, 1e4, None) == ERR_ARG
     assert lib.jepa_linear(C.c_void_p(16), C.c_void_p(16), None, C.c_void_p(16), 8, 32, 40, 2, 0, None) == ERR_ARG
+    # tensor-core widths are whole 128-column tiles
+    assert lib.jepa_linear(C.c_void_p(16), C.c_void_p(16), None, C.c_void_p(16), 8, 96, 64, 2, 0, None) == ERR_ARG
     assert lib.jepa_attention(C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), 2, 1, 1, 100, 64,
                               100, 0.125, None) == ERR_ARG          # ldv not a multiple of 8
     v = C.c_void_p(16)

@@ -102,11 +102,10 @@ def test_linear(jg, dtype, epi, M, N, K):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("epi", [0, 1, 2, 3])
-@pytest.mark.parametrize("M,N,K", [(1, 32, 64), (3, 96, 64), (129, 160, 192), (300, 224, 128)])
-def test_linear_ragged_width_and_tiny(jg, dtype, epi, M, N, K):
-    """Output widths that leave the last 128-column tile partly (96, 160,
-    224 columns) or mostly (32) outside the output, with a bias of exactly N
-    values; one and three rows; a single K block."""
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (3, 384, 64), (129, 128, 192), (300, 640, 128)])
+def test_linear_few_rows(jg, dtype, epi, M, N, K):
+    """One, three and 129 rows (a row tile of 128 plus one), a single K
+    block, a 384-wide output (128-column tiles) and 640 (256 + 256 + 128)."""
     rng = np.random.default_rng(M * 7 + N + K + epi)
     A = _rounded(rng, (M, K), dtype)
     W = _rounded(rng, (N, K), dtype, 0.05)
@@ -120,6 +119,22 @@ def test_linear_ragged_width_and_tiny(jg, dtype, epi, M, N, K):
         assert m["rel_max"] <= (1e-5 if dtype == "f32" else 1e-4), (dtype, epi, m)
     else:
         assert_close_16bit(got, ref, f"linear {dtype} epi {epi} M{M} N{N}")
+
+
+@pytest.mark.parametrize("epi", [0, 1, 2, 3])
+@pytest.mark.parametrize("N", [32, 96, 160, 224])
+def test_linear_f32_ragged_width(jg, epi, N):
+    """The fp32 path takes any width that is a multiple of 4 (the tensor-core
+    path refuses widths that are not whole 128-column tiles)."""
+    M, K, dtype = 70, 48, "f32"
+    rng = np.random.default_rng(N + epi)
+    A = _rounded(rng, (M, K), dtype)
+    W = _rounded(rng, (N, K), dtype, 0.05)
+    b = rng.standard_normal(N).astype(np.float32).astype(np.float64) * 0.1
+    resid = rng.standard_normal((M, N)).astype(np.float32).astype(np.float64)
+    out = _dev(resid) if epi == 2 else None
+    got = jg.linear(_dev(A, dtype), _dev(W, dtype), _dev(b), epi, out=out).float().cpu().numpy()
+    assert metrics(got, _linear_ref(A, W, b, epi, resid))["rel_max"] <= 1e-5
 
 
 @pytest.mark.parametrize("epi", [1, 2, 3])

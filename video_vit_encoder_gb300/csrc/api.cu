@@ -167,8 +167,10 @@ jepa_status check_width(int D, int H, int F, int dtype, const char* who) {
   const int hd = D / H;
   if (hd != 32 && hd != 64) return fail(JEPA_ERR_UNSUPPORTED, "%s: head_dim %d (supported: 32, 64)", who, hd);
   if (D % 128 != 0 || D > 4096) return fail(JEPA_ERR_UNSUPPORTED, "%s: embed_dim %d must be a multiple of 128, <= 4096", who, D);
-  if (F % 64 != 0) return fail(JEPA_ERR_UNSUPPORTED, "%s: ffn_dim %d must be a multiple of 64", who, F);
   if (dtype < 0 || dtype > 2) return fail(JEPA_ERR_ARG, "%s: bad dtype %d", who, dtype);
+  // the tensor-core GEMMs take whole 128-column output tiles
+  if (F % (dtype == DTYPE_F32 ? 64 : 128) != 0)
+    return fail(JEPA_ERR_UNSUPPORTED, "%s: ffn_dim %d must be a multiple of %d", who, F, dtype == DTYPE_F32 ? 64 : 128);
   return JEPA_OK;
 }
 
@@ -193,7 +195,8 @@ jepa_status check_predictor_params(const jepa_predictor_params* p) {
   if (p == nullptr) return fail(JEPA_ERR_ARG, "params is NULL");
   JEPA_TRY(check_width(p->embed_dim, p->n_head, p->ffn_dim, p->dtype, "predictor"));
   if (p->in_dim <= 0 || p->in_dim % 64 != 0) return fail(JEPA_ERR_UNSUPPORTED, "in_dim %d must be a multiple of 64", p->in_dim);
-  if (p->out_dim <= 0 || p->out_dim % 32 != 0) return fail(JEPA_ERR_UNSUPPORTED, "out_dim %d must be a multiple of 32", p->out_dim);
+  if (p->out_dim <= 0 || p->out_dim % (p->dtype == DTYPE_F32 ? 32 : 128) != 0)
+    return fail(JEPA_ERR_UNSUPPORTED, "out_dim %d must be a multiple of %d", p->out_dim, p->dtype == DTYPE_F32 ? 32 : 128);
   if (p->n_mask_tokens <= 0 || p->mask_index < 0) return fail(JEPA_ERR_ARG, "mask tokens");
   if (p->rope_layout != 0 && p->rope_layout != 1) return fail(JEPA_ERR_ARG, "rope_layout %d", p->rope_layout);
   if (p->n_layer < 0) return fail(JEPA_ERR_ARG, "n_layer %d", p->n_layer);
@@ -1450,8 +1453,8 @@ jepa_status jepa_linear(const void* A, const void* W, const float* bias, void* o
   if (M < 0 || N <= 0 || K <= 0) return fail(JEPA_ERR_ARG, "M %d N %d K %d", M, N, K);
   if (dtype == DTYPE_F32 && (K % 16 != 0 || N % 4 != 0))
     return fail(JEPA_ERR_ARG, "fp32 linear needs K %% 16 == 0 and N %% 4 == 0");
-  if (dtype != DTYPE_F32 && (K % 64 != 0 || N % 32 != 0))
-    return fail(JEPA_ERR_ARG, "tensor-core linear needs K %% 64 == 0 and N %% 32 == 0");
+  if (dtype != DTYPE_F32 && (K % 64 != 0 || N % 128 != 0))
+    return fail(JEPA_ERR_ARG, "tensor-core linear needs K %% 64 == 0 and N %% 128 == 0");
   int* st = nullptr;
   JEPA_TRY(ops_status(&st));
   int dev = 0, sms = 0;
@@ -1472,7 +1475,7 @@ jepa_status jepa_qkv_rope(const void* A, const void* W, const float* bias, void*
   if (!aligned16(A) || !aligned16(W) || !aligned16(bias) || !aligned16(q) || !aligned16(k) || !aligned16(vt))
     return fail(JEPA_ERR_ARG, "buffers must be 16-byte aligned");
   if (dtype < 0 || dtype > 2) return fail(JEPA_ERR_ARG, "dtype %d", dtype);
-  JEPA_TRY(check_width(embed_dim, n_head, 64, dtype, "qkv_rope"));
+  JEPA_TRY(check_width(embed_dim, n_head, 128, dtype, "qkv_rope"));   // this call has no FFN: 128 passes its check
   const int hd = embed_dim / n_head;
   if (batch < 1 || n_tokens < 1) return fail(JEPA_ERR_ARG, "batch %d and n_tokens %d must be >= 1", batch, n_tokens);
   if (grid_t < 1 || grid_h < 1 || grid_w < 1) return fail(JEPA_ERR_ARG, "grid %dx%dx%d", grid_t, grid_h, grid_w);
