@@ -200,14 +200,12 @@ __device__ __forceinline__ void qkv_tile_epilogue(const EpiParams& ep, uint32_t 
 // output, which holds the residual: out = residual + (accumulator + bias),
 // one fp32 addition per element performed by L2.  The warp's next block waits
 // only until the previous reduction has read the buffer, not for its writes.
-// n_cols: output columns that exist from col0 (N - col0); blocks past them
-// are skipped and the bias is read only inside them.
 template <int NCOLS>
 __device__ __forceinline__ void reduce_epilogue(const EpiParams& ep, const CUtensorMap* tmC, uint32_t taddr, int row0,
-                                                int col0, int n_cols, uint8_t* buf, int lane) {
+                                                int col0, uint8_t* buf, int lane) {
   constexpr int kCols = 32;  // fp32 columns per 128-byte block
 #pragma unroll 1
-  for (int c = 0; c < NCOLS / kCols && c * kCols < n_cols; ++c) {
+  for (int c = 0; c < NCOLS / kCols; ++c) {
     float v[kCols];
     {
       uint32_t r[32];
@@ -220,7 +218,7 @@ __device__ __forceinline__ void reduce_epilogue(const EpiParams& ep, const CUten
       const float4* b4 = reinterpret_cast<const float4*>(ep.bias + col0 + c * kCols);
 #pragma unroll
       for (int i = 0; i < kCols / 4; ++i) {
-        const float4 bb = c * kCols + 4 * i < n_cols ? __ldg(b4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 bb = __ldg(b4 + i);
         add2f(v[4 * i], v[4 * i + 1], bb.x, bb.y);
         add2f(v[4 * i + 2], v[4 * i + 3], bb.z, bb.w);
       }
@@ -249,13 +247,13 @@ __device__ __forceinline__ void reduce_epilogue(const EpiParams& ep, const CUten
 // per lane.  Rows and columns outside the output are clipped by the tensor map.
 template <typename T, int EPI, int NCOLS>
 __device__ __forceinline__ void staged_epilogue(const EpiParams& ep, const CUtensorMap* tmC, uint32_t taddr, int row0,
-                                                int col0, int n_cols, uint8_t* buf, int lane) {
+                                                int col0, uint8_t* buf, int lane) {
   static_assert(EPI == EPI_STORE || EPI == EPI_F32 || EPI == EPI_GELU, "staged epilogue");
   constexpr bool kF32Out = EPI == EPI_F32;
   constexpr int kCols = kF32Out ? 32 : 64;  // columns per 128-byte block
   uint8_t* my_row = buf + lane * 128;
 #pragma unroll 1
-  for (int c0 = 0; c0 < NCOLS && c0 < n_cols; c0 += kCols) {
+  for (int c0 = 0; c0 < NCOLS; c0 += kCols) {
     float v[kCols];
 #pragma unroll
     for (int h = 0; h < kCols / 32; ++h) {
@@ -269,7 +267,7 @@ __device__ __forceinline__ void staged_epilogue(const EpiParams& ep, const CUten
       const float4* b4 = reinterpret_cast<const float4*>(ep.bias + col0 + c0);
 #pragma unroll
       for (int i = 0; i < kCols / 4; ++i) {
-        const float4 bb = c0 + 4 * i < n_cols ? __ldg(b4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 bb = __ldg(b4 + i);
         add2f(v[4 * i], v[4 * i + 1], bb.x, bb.y);
         add2f(v[4 * i + 2], v[4 * i + 3], bb.z, bb.w);
       }
@@ -544,20 +542,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                stage_buf, M, lane, wcols / 32);
       } else if (ut.width == BN) {
         if constexpr (EPI == EPI_RESID) {
-          reduce_epilogue<BN / 2>(ep, &tmC, tlane + half * (BN / 2), row - lane, ut.col0 + half * (BN / 2),
-                                  N - (ut.col0 + half * (BN / 2)), stage_buf, lane);
+          reduce_epilogue<BN / 2>(ep, &tmC, tlane + half * (BN / 2), row - lane, ut.col0 + half * (BN / 2), stage_buf,
+                                  lane);
         } else {
           staged_epilogue<T, EPI, BN / 2>(ep, &tmC, tlane + half * (BN / 2), row - lane, ut.col0 + half * (BN / 2),
-                                          N - (ut.col0 + half * (BN / 2)), stage_buf, lane);
+                                          stage_buf, lane);
         }
       } else if constexpr (can_split_tail<BN, EPI, QHD>()) {
         // half-width tail tile: each warp drains BN/4 columns
         if constexpr (EPI == EPI_RESID) {
-          reduce_epilogue<BN / 4>(ep, &tmC, tlane + half * (BN / 4), row - lane, ut.col0 + half * (BN / 4),
-                                  N - (ut.col0 + half * (BN / 4)), stage_buf, lane);
+          reduce_epilogue<BN / 4>(ep, &tmC, tlane + half * (BN / 4), row - lane, ut.col0 + half * (BN / 4), stage_buf,
+                                  lane);
         } else {
           staged_epilogue<T, EPI, BN / 4>(ep, &tmC, tlane + half * (BN / 4), row - lane, ut.col0 + half * (BN / 4),
-                                          N - (ut.col0 + half * (BN / 4)), stage_buf, lane);
+                                          stage_buf, lane);
         }
       }
       tc_fence_before();
