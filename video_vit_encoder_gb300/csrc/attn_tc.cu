@@ -702,14 +702,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tile is done (at a unit's first key tile: the previous unit's last).
         if (g >= 1 && !mbar_wait(&pv_done[t], (g - 1) & 1)) ok = false;
         tc_fence_after();
-        if (j == 0 && k >= 1) {  // the previous unit's output, before this unit's first P V replaces O_t
-          const int pu = (int)blockIdx.x + (k - 1) * (int)gridDim.x;
-          const int pbh = pu / n_qp, pq0 = (pu - pbh * n_qp) * 2 * kBQ;
-          store_o_rows<T, HD>(&tmO, tO, l_prev,
-                              sQ + ((k - 1) & 1) * 2 * S::kQBytes + t * S::kQBytes + quarter * 32 * kQKRow, lane,
-                              pbh % n_head, pq0 + t * kBQ + quarter * 32, pbh / n_head);
-          staged = true;
-        }
         // Move the running max of the warp's rows when any grew by more than 2^8
         // (in the exponent): O_t and l are rescaled by 2^((m_old - m_new) scale log2e).
         if (__any_sync(0xffffffffu, j > 0 && (mx - m) * scale_log2 > 8.0f)) {
@@ -740,6 +732,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    : exp_to_tmem<T, true>(sv, kvalid, scale_log2, -m * scale_log2, tP);
         l += rs;
         mbar_arrive(&exp_tok[t * 4 + quarter]);
+        // The previous unit's output, read before this unit's first P V
+        // replaces O_t (that P V waits for p_full) and after this tile's
+        // exponentials, when the score registers are free.
+        if (j == 0 && k >= 1) {
+          const int pu = (int)blockIdx.x + (k - 1) * (int)gridDim.x;
+          const int pbh = pu / n_qp, pq0 = (pu - pbh * n_qp) * 2 * kBQ;
+          store_o_rows<T, HD>(&tmO, tO, l_prev,
+                              sQ + ((k - 1) & 1) * 2 * S::kQBytes + t * S::kQBytes + quarter * 32 * kQKRow, lane,
+                              pbh % n_head, pq0 + t * kBQ + quarter * 32, pbh / n_head);
+          staged = true;
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
