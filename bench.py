@@ -39,26 +39,28 @@ sys.path.insert(0, ROOT)
 UNIT = "tokens/s"
 # name -> (seeded config, metric, workload description, fraction of tokens kept or None)
 WORKLOADS = {
-    "vitl16-16f256": ("c3", "encoder tokens/sec (ViT-L/16, 16f 256px, bf16) and % of bf16 tensor peak",
+    "vitl16-16f256": ("vitl16-16f256", "encoder tokens/sec (ViT-L/16, 16f 256px, bf16) and % of bf16 tensor peak",
                       "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 16f x 256x256 (2048 tokens/clip), "
                       "batch 8 per GPU", None),
-    "vitl16-16f256-masked50": ("c3", "masked-encoder kept tokens/sec (ViT-L/16, 16f 256px, half the tokens kept, "
-                               "bf16) and % of bf16 tensor peak",
+    "vitl16-16f256-masked50": ("vitl16-16f256", "masked-encoder kept tokens/sec (ViT-L/16, 16f 256px, half the "
+                               "tokens kept, bf16) and % of bf16 tensor peak",
                                "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 16f x 256x256, masked encoder "
                                "forward keeping a seeded random 1024 of each clip's 2048 tokens, batch 8 per GPU", 0.5),
     "vitb16-img384": ("img384", "encoder tokens/sec (V-JEPA 2.1 ViT-B/16 native image path, 384px, bf16) and % of "
                       "bf16 tensor peak",
                       "ViT-B/16 12L D768 h12 FFN3072, bf16, 2.1 native image path (tubelet 1, patch_embed_img), "
                       "interleaved interpolated RoPE, 1f x 384x384 (576 tokens/image), batch 32 per GPU", None),
-    "vitl16-16f256-ssv2": ("c3", "classified tokens/sec (ViT-L/16 encoder + SSv2 attentive-pool head and 174-class "
-                           "classifier, 16f 256px, bf16) and % of bf16 tensor peak",
+    "vitl16-16f256-ssv2": ("vitl16-16f256", "classified tokens/sec (ViT-L/16 encoder + SSv2 attentive-pool head "
+                           "and 174-class classifier, 16f 256px, bf16) and % of bf16 tensor peak",
                            "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 16f x 256x256 (2048 tokens/clip), then the "
                            "attentive-pool head (3 pool blocks, 16 heads, single-query cross-attention, 174 classes), "
                            "batch 8 per GPU", None),
-    "vitl16-64f256": ("c4", "encoder tokens/sec (ViT-L/16, 64f 256px, bf16) and % of bf16 tensor peak",
+    "vitl16-64f256": ("vitl16-64f256-pred", "encoder tokens/sec (ViT-L/16, 64f 256px, bf16) and % of bf16 tensor "
+                      "peak",
                       "ViT-L/16 24L D1024 h16 FFN4096, bf16, tiled RoPE, 64f x 256x256 (8192 tokens/clip), "
                       "batch 1 per GPU", None),
-    "vitb16-64f384": ("c5", "encoder tokens/sec (V-JEPA 2.1 ViT-B/16, 64f 384px, bf16) and % of bf16 tensor peak",
+    "vitb16-64f384": ("vitb16-64f384", "encoder tokens/sec (V-JEPA 2.1 ViT-B/16, 64f 384px, bf16) and % of bf16 "
+                      "tensor peak",
                       "ViT-B/16 12L D768 h12 FFN3072, bf16, interleaved interpolated RoPE, 64f x 384x384 "
                       "(18432 tokens/clip), batch 1 per GPU", None),
 }

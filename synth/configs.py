@@ -100,26 +100,28 @@ def tokens_per_clip(cfg: EncoderConfig) -> int:
 
 
 CONFIGS = {
-    "c1": EncoderConfig(
-        name="c1", workload="single block + patch embed, fp32, D768 h12, 4f 128px (128 tokens), batch 1",
+    "block-f32-4f128": EncoderConfig(
+        name="block-f32-4f128", workload="single block + patch embed, fp32, D768 h12, 4f 128px (128 tokens), batch 1",
         embed_dim=768, n_layer=1, n_head=12, ffn_dim=3072, n_frames=4, height=128, width=128,
         batch=1, dtype="f32", rope_layout="tiled", rope_interpolate=False, seed=0),
-    "c2": EncoderConfig(
-        name="c2", workload="ViT-B/16 12L, fp16, interleaved interpolated RoPE, 16f 384px (4608 tokens), batch 1",
+    "vitb16-16f384-f16": EncoderConfig(
+        name="vitb16-16f384-f16",
+        workload="ViT-B/16 12L, fp16, interleaved interpolated RoPE, 16f 384px (4608 tokens), batch 1",
         embed_dim=768, n_layer=12, n_head=12, ffn_dim=3072, n_frames=16, height=384, width=384,
         batch=1, dtype="f16", rope_layout="interleaved", rope_interpolate=True, seed=1,
         has_mod_embed=True),
-    "c3": EncoderConfig(
-        name="c3", workload="ViT-L/16 24L, bf16, tiled RoPE, 16f 256px (2048 tokens/clip), batch 8",
+    "vitl16-16f256": EncoderConfig(
+        name="vitl16-16f256", workload="ViT-L/16 24L, bf16, tiled RoPE, 16f 256px (2048 tokens/clip), batch 8",
         embed_dim=1024, n_layer=24, n_head=16, ffn_dim=4096, n_frames=16, height=256, width=256,
         batch=8, dtype="bf16", rope_layout="tiled", rope_interpolate=False, seed=2),
-    "c4": EncoderConfig(
-        name="c4", workload="ViT-L/16 24L, bf16, 64f 256px (8192 tokens), batch 1, + masked predictor",
+    "vitl16-64f256-pred": EncoderConfig(
+        name="vitl16-64f256-pred", workload="ViT-L/16 24L, bf16, 64f 256px (8192 tokens), batch 1, + masked predictor",
         embed_dim=1024, n_layer=24, n_head=16, ffn_dim=4096, n_frames=64, height=256, width=256,
         batch=1, dtype="bf16", rope_layout="tiled", rope_interpolate=False, seed=3,
         predictor=PredictorConfig()),
-    "c5": EncoderConfig(
-        name="c5", workload="ViT-B/16 12L, bf16, interleaved interpolated RoPE, 64f 384px (18432 tokens), batch 1, hier taps",
+    "vitb16-64f384": EncoderConfig(
+        name="vitb16-64f384",
+        workload="ViT-B/16 12L, bf16, interleaved interpolated RoPE, 64f 384px (18432 tokens), batch 1, hier taps",
         embed_dim=768, n_layer=12, n_head=12, ffn_dim=3072, n_frames=64, height=384, width=384,
         batch=1, dtype="bf16", rope_layout="interleaved", rope_interpolate=True, seed=4,
         hier_layers=(2, 5, 8, 11), has_mod_embed=True),

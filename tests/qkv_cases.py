@@ -117,10 +117,10 @@ def reference(case, A, W, b, ids, layout=None, interp=None, mode="ids"):
 SHARP_QKV_STD = 0.108
 SHARP_MODELS = {
     # V-JEPA 2 geometry: tiled RoPE, head_dim 32, N = 3*5*9 = 135 (ragged against 128-row tiles)
-    "v2-hd32-sharp": synth.CONFIGS["c3"].with_(embed_dim=256, n_head=8, ffn_dim=512, n_layer=2, n_frames=6,
+    "v2-hd32-sharp": synth.CONFIGS["vitl16-16f256"].with_(embed_dim=256, n_head=8, ffn_dim=512, n_layer=2, n_frames=6,
                                                height=80, width=144, batch=2),
     # 2.1 geometry: interleaved RoPE interpolated to the 16-grid, modality vector, taps; N = 2*6*8 = 96
-    "b21-hd64-sharp": synth.CONFIGS["c5"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=3, n_frames=4,
+    "b21-hd64-sharp": synth.CONFIGS["vitb16-64f384"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=3, n_frames=4,
                                                 height=96, width=128, batch=2, hier_layers=(0, 2)),
 }
 

@@ -45,7 +45,7 @@ def _blob(cfg):
 def test_blob_roundtrip_and_faults(lib):
     import video_vit_encoder_gb300 as jg
     from video_vit_encoder_gb300._lib import JepaError, ERR_BLOB, ERR_ARG, ERR_UNSUPPORTED
-    cfg = synth.CONFIGS["c1"].with_(n_layer=2, dtype="bf16")
+    cfg = synth.CONFIGS["block-f32-4f128"].with_(n_layer=2, dtype="bf16")
     blob = _blob(cfg)
     jg.blob_check(cfg, blob)                       # valid
     with pytest.raises(JepaError) as e:            # truncated
@@ -89,7 +89,7 @@ def test_blob_with_image_path(lib):
 
 def test_blob_layout_is_aligned(lib):
     import struct
-    cfg = synth.CONFIGS["c1"].with_(dtype="f16")
+    cfg = synth.CONFIGS["block-f32-4f128"].with_(dtype="f16")
     blob = _blob(cfg)
     assert blob[:8] == b"JEPAGB3\0"
     ver, n = struct.unpack_from("<II", blob, 8)

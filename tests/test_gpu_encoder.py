@@ -23,12 +23,12 @@ def jg():
 
 SMALL = {
     # 2.1 geometry: interleaved interpolated RoPE, modality vector, hierarchical taps; N = 2*6*8 = 96
-    "b21-bf16": synth.CONFIGS["c5"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=3, n_frames=4,
+    "b21-bf16": synth.CONFIGS["vitb16-64f384"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=3, n_frames=4,
                                           height=96, width=128, batch=3, hier_layers=(0, 2)),
-    "b21-f16": synth.CONFIGS["c2"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=3, n_frames=4,
+    "b21-f16": synth.CONFIGS["vitb16-16f384-f16"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=3, n_frames=4,
                                          height=96, width=128, batch=2, hier_layers=(1,)),
     # V-JEPA 2 geometry, tiled RoPE, head_dim 32, N = 3*5*9 = 135 (ragged against 128-row tiles)
-    "v2-hd32": synth.CONFIGS["c3"].with_(embed_dim=256, n_head=8, ffn_dim=512, n_layer=2, n_frames=6,
+    "v2-hd32": synth.CONFIGS["vitl16-16f256"].with_(embed_dim=256, n_head=8, ffn_dim=512, n_layer=2, n_frames=6,
                                          height=80, width=144, batch=2),
     # 2.1 native image path (one frame, tubelet 1), N = 6*8 = 48 and 11*5 = 55
     "img21-bf16": synth.CONFIGS["img384"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=3, height=96,
@@ -36,9 +36,9 @@ SMALL = {
     "img21-f16": synth.CONFIGS["img384"].with_(embed_dim=256, n_head=4, ffn_dim=1024, n_layer=2, height=176,
                                                width=80, batch=2, dtype="f16", hier_layers=(1,)),
     # the smallest clips: one token (2 frames of 16 x 16), and two tokens along t
-    "v2-1tok": synth.CONFIGS["c3"].with_(embed_dim=256, n_head=4, ffn_dim=512, n_layer=2, n_frames=2,
+    "v2-1tok": synth.CONFIGS["vitl16-16f256"].with_(embed_dim=256, n_head=4, ffn_dim=512, n_layer=2, n_frames=2,
                                          height=16, width=16, batch=3),
-    "v2-2tok": synth.CONFIGS["c3"].with_(embed_dim=256, n_head=4, ffn_dim=512, n_layer=2, n_frames=4,
+    "v2-2tok": synth.CONFIGS["vitl16-16f256"].with_(embed_dim=256, n_head=4, ffn_dim=512, n_layer=2, n_frames=4,
                                          height=16, width=16, batch=2),
 }
 
@@ -65,12 +65,12 @@ def test_small_end_to_end(jg, name):
     enc.close()
 
 
-def test_c1_fp32_end_to_end(jg):
-    cfg = synth.CONFIGS["c1"]
+def test_block_f32_4f128_fp32_end_to_end(jg):
+    cfg = synth.CONFIGS["block-f32-4f128"]
     enc, w, clip, got = _run(jg, cfg, hier=False)
     ref = oracle.encoder_forward(cfg, w, clip[0])
-    m = assert_close_f32(got["out"][0], ref["out"], REL_F32_PATH, "c1")
-    print("c1 parity", m)
+    m = assert_close_f32(got["out"][0], ref["out"], REL_F32_PATH, "block-f32-4f128")
+    print("block-f32-4f128 parity", m)
     enc.close()
 
 

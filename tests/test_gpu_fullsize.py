@@ -1,15 +1,15 @@
 """Full-size workloads on the GPU against the oracle.
 
 At these sizes the oracle checks what it can compute in seconds:
-  * c3 (ViT-L/16, 8 clips of 16x256x256, the benchmark's launch) - clip 0 end
+  * vitl16-16f256 (ViT-L/16, 8 clips of 16x256x256, the benchmark's launch) - clip 0 end
     to end on every token, clip 7 block by block on sampled rows;
   * img384 (2.1 native image path, 32 images of 384 px) - two images end to
     end on every token, with the hierarchical taps;
-  * c2 (2.1 ViT-B/16, fp16, one 16 x 384 x 384 clip) - end to end on every
+  * vitb16-16f384-f16 (2.1 ViT-B/16, fp16, one 16 x 384 x 384 clip) - end to end on every
     token, and block by block on sampled rows;
-  * c4, c5 - block by block on sampled rows (each block recomputed by the
+  * vitl16-64f256-pred, vitb16-64f384 - block by block on sampled rows (each block recomputed by the
     oracle from the GPU's own input residual), the final norm and the
-    hierarchical taps on sampled rows, and the c4 predictor end to end.
+    hierarchical taps on sampled rows, and the predictor end to end.
 """
 import numpy as np
 import pytest
@@ -70,36 +70,36 @@ def _check_blocks(enc, cfg, w, clip_t, clip_idx, n_rows, seed, stats):
     return x, rows
 
 
-def test_c3_clip0_end_to_end(jg):
-    cfg = synth.CONFIGS["c3"]
-    w = _weights("c3")
+def test_vitl16_16f256_clip0_end_to_end(jg):
+    cfg = synth.CONFIGS["vitl16-16f256"]
+    w = _weights("vitl16-16f256")
     clip = synth.clip_u8(cfg)
     enc = jg.Encoder(cfg, w)
     res = enc.encode(torch.from_numpy(clip).cuda(), pooled=True)
     enc.sync()
     out = res["out"].cpu().numpy()
     ref = oracle.encoder_forward(cfg, w, clip[0])
-    m = assert_close_16bit(out[0], ref["out"], "c3 clip 0")
-    print("c3 clip 0 end to end:", m)
+    m = assert_close_16bit(out[0], ref["out"], "vitl16-16f256 clip 0")
+    print("vitl16-16f256 clip 0 end to end:", m)
     np.testing.assert_allclose(res["pooled"][0].cpu().numpy(), ref["pooled"], atol=1e-2 * np.abs(ref["pooled"]).max())
     enc.close()
 
 
-def test_c3_clip7_blocks(jg):
-    cfg = synth.CONFIGS["c3"]
-    w = _weights("c3")
+def test_vitl16_16f256_clip7_blocks(jg):
+    cfg = synth.CONFIGS["vitl16-16f256"]
+    w = _weights("vitl16-16f256")
     clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
     enc = jg.Encoder(cfg, w)
     stats = []
     x, rows = _check_blocks(enc, cfg, w, clip, 7, 48, 3, stats)
-    print("c3 clip 7 per-block delta worst cos:", min(s[1]["cos_worst"] for s in stats),
+    print("vitl16-16f256 clip 7 per-block delta worst cos:", min(s[1]["cos_worst"] for s in stats),
           "max rel:", max(s[1]["rel_max"] for s in stats))
     enc.close()
 
 
-def test_c2_blocks_and_final(jg):
-    cfg = synth.CONFIGS["c2"]
-    w = _weights("c2")
+def test_vitb16_16f384_f16_blocks_and_final(jg):
+    cfg = synth.CONFIGS["vitb16-16f384-f16"]
+    w = _weights("vitb16-16f384-f16")
     clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
     enc = jg.Encoder(cfg, w)
     stats = []
@@ -108,31 +108,31 @@ def test_c2_blocks_and_final(jg):
     enc.sync()
     xr = x.cpu().numpy().astype(np.float64)[rows]
     ref = oracle.layer_norm(xr, w["norm.weight"], w["norm.bias"], cfg.ln_eps)
-    assert_close_16bit(out[0].cpu().numpy()[rows], ref, "c2 final norm")
+    assert_close_16bit(out[0].cpu().numpy()[rows], ref, "vitb16-16f384-f16 final norm")
     enc.close()
 
 
-def test_c2_end_to_end(jg):
+def test_vitb16_16f384_f16_end_to_end(jg):
     """The 2.1 ViT-B/16 fp16 workload (12 layers, interleaved RoPE
     interpolated to the 16-grid, modality vector, one 16 x 384 x 384 clip of
     4608 tokens) end to end on every token against the oracle, so error that
     grows through the 12 layers is compared too."""
-    cfg = synth.CONFIGS["c2"]
-    w = _weights("c2")
+    cfg = synth.CONFIGS["vitb16-16f384-f16"]
+    w = _weights("vitb16-16f384-f16")
     clip = synth.clip_u8(cfg)
     enc = jg.Encoder(cfg, w)
     res = enc.encode(torch.from_numpy(clip).cuda(), pooled=True)
     enc.sync()
     ref = oracle.encoder_forward(cfg, w, clip[0])
-    m = assert_close_16bit(res["out"][0].cpu().numpy(), ref["out"], "c2 end to end")
-    print("c2 end to end:", m)
+    m = assert_close_16bit(res["out"][0].cpu().numpy(), ref["out"], "vitb16-16f384-f16 end to end")
+    print("vitb16-16f384-f16 end to end:", m)
     np.testing.assert_allclose(res["pooled"][0].cpu().numpy(), ref["pooled"], atol=1e-2 * np.abs(ref["pooled"]).max())
     enc.close()
 
 
-def test_c5_blocks_taps_final(jg):
-    cfg = synth.CONFIGS["c5"]
-    w = _weights("c5")
+def test_vitb16_64f384_blocks_taps_final(jg):
+    cfg = synth.CONFIGS["vitb16-64f384"]
+    w = _weights("vitb16-64f384")
     clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
     enc = jg.Encoder(cfg, w)
     res = enc.encode(clip, hier=True)
@@ -150,16 +150,16 @@ def test_c5_blocks_taps_final(jg):
         enc.sync()
         xr = x_l.view(N, D).cpu().numpy().astype(np.float64)[rows]
         ref = oracle.layer_norm(xr, w[f"hier_norm.{k}.weight"], w[f"hier_norm.{k}.bias"], cfg.ln_eps)
-        assert_close_16bit(res["hier"][k, 0].cpu().numpy()[rows], ref, f"c5 tap {k}")
+        assert_close_16bit(res["hier"][k, 0].cpu().numpy()[rows], ref, f"vitb16-64f384 tap {k}")
     ref = oracle.layer_norm(x_l.view(N, D).cpu().numpy().astype(np.float64)[rows], w["norm.weight"], w["norm.bias"],
                             cfg.ln_eps)
-    assert_close_16bit(res["out"][0].cpu().numpy()[rows], ref, "c5 final norm")
+    assert_close_16bit(res["out"][0].cpu().numpy()[rows], ref, "vitb16-64f384 final norm")
     enc.close()
 
 
-def test_c4_encoder_blocks_and_predictor(jg):
-    cfg = synth.CONFIGS["c4"]
-    w = _weights("c4")
+def test_vitl16_64f256_pred_encoder_blocks_and_predictor(jg):
+    cfg = synth.CONFIGS["vitl16-64f256-pred"]
+    w = _weights("vitl16-64f256-pred")
     clip = torch.from_numpy(synth.clip_u8(cfg)).cuda()
     enc = jg.Encoder(cfg, w)
     stats = []
@@ -174,8 +174,8 @@ def test_c4_encoder_blocks_and_predictor(jg):
     out = pred.predict(tokens, torch.from_numpy(ctx).cuda(), torch.from_numpy(tgt).cuda(), cfg.grid())
     pred.sync()
     ref = oracle.predictor_forward(pc, pw, tokens.cpu().numpy().astype(np.float64), ctx, tgt, cfg.grid())
-    m = assert_close_16bit(out.cpu().numpy(), ref, "c4 predictor")
-    print("c4 predictor:", m)
+    m = assert_close_16bit(out.cpu().numpy(), ref, "vitl16-64f256-pred predictor")
+    print("vitl16-64f256-pred predictor:", m)
     pred.close()
 
 
@@ -232,12 +232,12 @@ def test_pred21_encoder_and_predictor(jg):
     enc.close()
 
 
-def test_c3_masked_encoder_clip0(jg):
+def test_vitl16_16f256_masked_encoder_clip0(jg):
     """Masked encoder forward at the ViT-L/16 16 x 256 x 256 geometry, batch 8,
     each clip keeping its own random half of the 2048 tokens; clip 0 end to end
     against the oracle's masked forward."""
-    cfg = synth.CONFIGS["c3"]
-    w = _weights("c3")
+    cfg = synth.CONFIGS["vitl16-16f256"]
+    w = _weights("vitl16-16f256")
     clip = synth.clip_u8(cfg)
     n = synth.tokens_per_clip(cfg)
     keep = np.stack([np.random.default_rng(40 + b).choice(n, n // 2, replace=False)
@@ -246,5 +246,5 @@ def test_c3_masked_encoder_clip0(jg):
     got = enc.encode_masked(torch.from_numpy(clip).cuda(), torch.from_numpy(keep).cuda())["out"]
     enc.sync()
     ref = oracle.encoder_forward(cfg, w, clip[0], keep=keep[0])
-    assert_close_16bit(got[0].cpu().numpy(), ref["out"], "c3 masked clip 0")
+    assert_close_16bit(got[0].cpu().numpy(), ref["out"], "vitl16-16f256 masked clip 0")
     enc.close()

@@ -92,7 +92,7 @@ def test_ssv2_head_on_vitl_encoder_output(jg):
     174 classes, bf16) on the ViT-L/16 encoder's own tokens for the
     benchmark's 8 clips of 16 x 256 x 256 (2048 tokens each); clips 0 and 7
     against the oracle run on the same tokens."""
-    cfg = synth.CONFIGS["c3"]
+    cfg = synth.CONFIGS["vitl16-16f256"]
     enc = jg.Encoder(cfg, synth.encoder_weights(cfg))
     tokens = enc.encode(torch.from_numpy(synth.clip_u8(cfg)).cuda())["out"]
     enc.sync()

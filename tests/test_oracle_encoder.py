@@ -15,8 +15,8 @@ import torch.nn.functional as Fn
 import oracle
 import synth
 
-C1 = synth.CONFIGS["c1"]
-SMALL_21 = synth.CONFIGS["c2"].with_(n_layer=2, n_frames=4, height=128, width=160, hier_layers=(0, 1),
+BLOCK_F32 = synth.CONFIGS["block-f32-4f128"]
+SMALL_21 = synth.CONFIGS["vitb16-16f384-f16"].with_(n_layer=2, n_frames=4, height=128, width=160, hier_layers=(0, 1),
                                      dtype="f32")
 
 
@@ -94,7 +94,7 @@ def _perturb_lns(w, seed):
     return w
 
 
-@pytest.mark.parametrize("cfg", [C1, SMALL_21], ids=["c1", "vitb21-2layer"])
+@pytest.mark.parametrize("cfg", [BLOCK_F32, SMALL_21], ids=["block-f32-4f128", "vitb21-2layer"])
 def test_encoder_matches_torch_composition(cfg):
     w = _perturb_lns(synth.encoder_weights(cfg), 7)
     clip = synth.clip_u8(cfg, batch=1)[0]
@@ -108,7 +108,7 @@ def test_encoder_matches_torch_composition(cfg):
 
 
 def test_zero_blocks_reduce_to_norm_of_patch_embed():
-    cfg = C1
+    cfg = BLOCK_F32
     w = synth.encoder_weights(cfg)
     for k in list(w):
         if k.startswith("blk."):
@@ -134,7 +134,7 @@ def test_block_rows_equals_full_block():
 
 def test_weight_perturbation_is_visible():
     # The parity gate must see a +1 % error on a single weight matrix.
-    cfg = C1
+    cfg = BLOCK_F32
     w = synth.encoder_weights(cfg)
     clip = synth.clip_u8(cfg, batch=1)[0]
     a = oracle.encoder_forward(cfg, w, clip)["out"]
@@ -144,7 +144,7 @@ def test_weight_perturbation_is_visible():
     assert np.max(np.abs(a - b)) / np.max(np.abs(a)) > 1e-4
 
 
-PRED_CFG = synth.CONFIGS["c4"].with_(
+PRED_CFG = synth.CONFIGS["vitl16-64f256-pred"].with_(
     n_frames=4, height=64, width=64,
     predictor=synth.PredictorConfig(n_layer=2, in_dim=1024))
 

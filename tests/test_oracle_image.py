@@ -101,7 +101,7 @@ def test_image_modality_vector_is_the_image_one():
 
 
 def test_one_frame_without_image_path_is_not_the_image_path():
-    cfg = synth.CONFIGS["c3"]
+    cfg = synth.CONFIGS["vitl16-16f256"]
     assert not oracle.is_image(cfg, 1)
     assert oracle.is_image(synth.CONFIGS["img384"], 1)
     assert not oracle.is_image(synth.CONFIGS["img384"], 2)

@@ -45,11 +45,11 @@ def test_bf16_and_f16_rounding_match_torch():
 
 def test_workload_shapes():
     c = synth.CONFIGS
-    assert synth.tokens_per_clip(c["c1"]) == 128
-    assert synth.tokens_per_clip(c["c3"]) == 2048
-    assert synth.tokens_per_clip(c["c4"]) == 8192
-    assert synth.tokens_per_clip(c["c5"]) == 18432
-    w = synth.encoder_weights(c["c1"])
+    assert synth.tokens_per_clip(c["block-f32-4f128"]) == 128
+    assert synth.tokens_per_clip(c["vitl16-16f256"]) == 2048
+    assert synth.tokens_per_clip(c["vitl16-64f256-pred"]) == 8192
+    assert synth.tokens_per_clip(c["vitb16-64f384"]) == 18432
+    w = synth.encoder_weights(c["block-f32-4f128"])
     assert w["patch_embed.weight"].shape == (768, 1536)
     assert w["blk.0.attn_qkv.weight"].shape == (2304, 768)
     assert np.all(w["blk.0.ln1.weight"] == 1) and np.all(w["blk.0.attn_qkv.bias"] == 0)

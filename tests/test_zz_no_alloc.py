@@ -39,7 +39,7 @@ def test_static_patch_embed_matches_oracle_and_encoder_embed(dtype):
     from video_vit_encoder_gb300._lib import DT_BF16, DT_F16, ERR_ARG, OK
     code = {"bf16": DT_BF16, "f16": DT_F16}[dtype]
     lib = jg.load()
-    cfg = synth.CONFIGS["c3"].with_(n_layer=1, dtype=dtype)     # ViT-L patch embedding
+    cfg = synth.CONFIGS["vitl16-16f256"].with_(n_layer=1, dtype=dtype)     # ViT-L patch embedding
     w = synth.encoder_weights(cfg)
     bias = np.random.default_rng(3).standard_normal(cfg.embed_dim).astype(np.float32) * 0.5
     w_b = dict(w, **{"patch_embed.bias": bias})

@@ -86,7 +86,7 @@ def _setup(op):
         # normalise + tubelet unfold + patch-embed GEMM of 8 clips of 16 x 256 x 256 (jepa_encoder_embed)
         import synth
         from . import binding
-        cfg = synth.CONFIGS["c3"].with_(n_layer=0)
+        cfg = synth.CONFIGS["vitl16-16f256"].with_(n_layer=0)
         enc = binding.Encoder(cfg, synth.encoder_weights(cfg))
         clip = torch.randint(0, 256, (B, 16, 256, 256, 3), dtype=torch.uint8, device="cuda", generator=g)
         return (lambda: enc.embed(clip)), 2.0 * M * 1536 * D, "TFLOP/s"
