@@ -670,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp stages its rows there and lane 0 stores them with one TMA tile
     // store, so the next unit's first key tile is not held up by global
     // stores.  The previous unit's output is taken at the next unit's first
-    // key tile, after that tile's score load and row max.
+    // key tile, after that tile's exponentials.
     bool ok = true;
     bool staged = false;  // the previous unit's rows are staged and their store not yet known to have read them
     float l_prev = 0.f;
